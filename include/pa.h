@@ -1,0 +1,170 @@
+/*
+ * pa.h -- C ABI of libpa.so: single-query paged-attention decode on GB300 (sm_103a).
+ *
+ * The operation. "vLLM's custom ROCm paged-attention kernel wins all sixty cells"
+ * (gqa-gate-costs-nothing), section 1, states the problem: pure decode, one query
+ * token per sequence and head, attending over a fully cached context. The context
+ * lives in a block-paged K/V cache addressed through a block table. For sequence b
+ * of length L = seq_lens[b], query head h and its KV head g(h) = h / G (G = Hq/Hkv):
+ *
+ *   s_t      = scale * dot(q[b,h,:], K[b,t,g(h),:])            t < L
+ *   out[b,h] = sum_t softmax(s)_t * V[b,t,g(h),:]
+ *
+ * where token t of sequence b is row (t % block_size) of physical block
+ * block_tables[b][t / block_size]. Slots at or past L (the unwritten tail of the
+ * last block, section 5 of the same page) are never read, so NaN there cannot
+ * reach the output. The context is split across CTAs and merged afterwards (the
+ * split-KV fix in "Hybrid-SSM decode rate on dual Radeon cards under vLLM"),
+ * with fp32 accumulation throughout and one rounding to the output type.
+ *
+ * Conventions for every call below.
+ *  - Pointers named q, k_cache, v_cache, block_tables, seq_lens, out, workspace
+ *    are DEVICE pointers, owned by the caller; the library never allocates, frees
+ *    or retains them, and keeps no state between calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) on the device current to the calling thread inside this library
+ *    (see pa_set_device). Host-side argument errors are returned synchronously
+ *    and nothing is launched.
+ *  - Layouts are dense, row-major, with no padding:
+ *        q, out        [B, Hq, D]                       (dtype)
+ *        k_cache,
+ *        v_cache       [num_blocks, block_size, Hkv, D] (dtype)
+ *        block_tables  [B, max_blocks_per_seq]          int32
+ *        seq_lens      [B]                              int32
+ *    q, k_cache, v_cache and out must be 16-byte aligned.
+ *  - Device-side problems (a block table entry outside [0, num_blocks) for a live
+ *    token, a seq_len that is negative or above max_seq_len or above
+ *    max_blocks_per_seq*block_size, a pipeline wait that gave up) never fault:
+ *    the kernel clamps, keeps going, and ORs a PA_DEVERR_* bit into the workspace
+ *    header; read it with pa_read_device_errors. The output of such a call is
+ *    finite but not meaningful.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0, G > 16 */
+  PA_ERR_UNSUPPORTED = 2,   /* head_dim not 128/256, or an option this build does not implement */
+  PA_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
+  PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed (the CUDA error is cleared) */
+  PA_ERR_OUT_OF_RANGE = 5   /* max_seq_len above max_blocks_per_seq * block_size, or a device error */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device error word (workspace header). */
+#define PA_DEVERR_BLOCK_INDEX 1u /* a live token's block table entry was outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 2u     /* a seq_len < 0, > max_seq_len or > max_blocks_per_seq*block_size */
+#define PA_DEVERR_TIMEOUT 4u     /* a shared-memory pipeline wait gave up (bounded spin) */
+
+typedef void* pa_stream_t; /* cudaStream_t */
+
+/* Largest query-head group (Hq / Hkv) a call accepts. */
+#define PA_MAX_GQA_GROUP 16
+
+/*
+ * Full argument set for pa_decode_ex. Fields beyond those of pa_decode:
+ *   splits  0 = choose the split count automatically (fill every SM even at batch 1);
+ *           > 0 = use at most this many splits of the context (tests, tuning).
+ * All other fields mean what the pa_decode parameters of the same name mean.
+ */
+typedef struct pa_decode_args {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  void* out;
+  int32_t B, Hq, Hkv, D;
+  int32_t block_size, num_blocks, max_blocks_per_seq, max_seq_len;
+  float scale;
+  int32_t dtype; /* pa_dtype */
+  int32_t splits;
+} pa_decode_args;
+
+/*
+ * Workspace bytes pa_decode needs for these sizes on the current device. The
+ * workspace holds the device error word, one counter per (sequence, KV head) and
+ * the fp32 split partials (m, l, acc). It must be zero-filled once before its first
+ * use (pa_workspace_init or any memset); every call leaves it ready for the next.
+ * Calls that overlap on the GPU must not share a workspace. max_seq_len <= 0 means
+ * max_blocks_per_seq * block_size is not known here: pass the real bound.
+ * Returns 0 for invalid sizes.
+ */
+size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size, int max_seq_len);
+
+/* Same, for pa_decode_ex's argument set (pointer fields are ignored). */
+size_t pa_decode_ex_workspace_bytes(const pa_decode_args* args);
+
+/*
+ * Single-query paged-attention decode.
+ *   q             [B, Hq, D] queries (dtype)
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, Hkv, D] paged keys / values (dtype)
+ *   block_tables  [B, max_blocks_per_seq] int32 physical block of each logical block;
+ *                 entries past ceil(seq_lens[b] / block_size) are never read
+ *   seq_lens      [B] int32 context length per sequence (0 gives a zero output row)
+ *   out           [B, Hq, D] output (dtype), fully written
+ *   B             batch (0 is a no-op), Hq and Hkv query and KV heads (Hq % Hkv == 0,
+ *                 Hq / Hkv <= PA_MAX_GQA_GROUP), D head_dim (128 or 256)
+ *   block_size    tokens per block (any positive size, e.g. 16 or 784)
+ *   num_blocks    blocks in each cache tensor
+ *   max_seq_len   a host-side upper bound on seq_lens (used to choose the split
+ *                 count without reading device memory); <= 0 means
+ *                 max_blocks_per_seq * block_size
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D))
+ *   dtype         PA_F16 or PA_BF16 for q, caches and out
+ *   workspace     device scratch of >= pa_decode_workspace_bytes(...) bytes,
+ *                 256-byte aligned, zero-filled before first use
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE,
+ * PA_ERR_OUT_OF_RANGE (max_seq_len above capacity), PA_ERR_CUDA.
+ */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                    int B, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                    int max_blocks_per_seq, int max_seq_len, float scale, pa_dtype dtype,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode with the extra options of pa_decode_args. Same errors. */
+pa_status pa_decode_ex(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream);
+
+/*
+ * The launch plan pa_decode_ex would use on a GPU with `sm_count` SMs: the number
+ * of context splits and the tokens per split (a multiple of 32). Pure host
+ * arithmetic; needs no GPU. sm_count <= 0 means the current device's SM count.
+ */
+pa_status pa_decode_plan(const pa_decode_args* args, int sm_count, int* splits,
+                         int* partition_tokens);
+
+/* Zero-fill a workspace on `stream` (asynchronous). */
+pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Wait for `stream`, then copy the device error word (PA_DEVERR_* bits) of
+ * `workspace` to *flags and clear it. Synchronous.
+ */
+pa_status pa_read_device_errors(void* workspace, pa_stream_t stream, uint32_t* flags);
+
+/* Make `device` current for this library's calls on the calling thread. */
+pa_status pa_set_device(int device);
+
+/* Static text for a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Library version, e.g. "0.1.0". */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,304 @@
+// Host side of libpa.so: argument validation, the split plan, the workspace
+// layout and the launch. Everything here is plain host code around one kernel
+// launch on the caller's stream; nothing synchronises with the device except
+// pa_read_device_errors.
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_params.h"
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t q) { return ceil_div(a, q) * q; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- split plan
+// Choose S (splits of each sequence's context) and P (tokens per split).
+// The unit of parallel work is a (sequence, KV head, split). With one resident
+// CTA per SM, S is chosen so that B * Hkv * S covers every SM, but no split gets
+// fewer than kPartitionMin tokens. P is a multiple of the 32-token warp tile and
+// small enough that a split's block-table slice fits the CTA's staging buffer.
+struct Plan {
+  int S;
+  int P;
+};
+
+bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t max_len,
+               int requested, Plan* out) {
+  if (max_len <= 0) {
+    *out = {1, pa::kTokenQuantum};
+    return true;
+  }
+  const int64_t units = B * Hkv;
+  int64_t S;
+  if (requested > 0) {
+    S = requested;
+  } else {
+    S = ceil_div(sm_count > 0 ? sm_count : 1, units);
+    S = std::min<int64_t>(S, ceil_div(max_len, pa::kPartitionMin));
+    S = std::max<int64_t>(S, 1);
+  }
+  S = std::min<int64_t>(S, ceil_div(max_len, pa::kTokenQuantum));
+  const int64_t p_max =
+      std::max<int64_t>(pa::kTokenQuantum,
+                        ((int64_t)(pa::kBtMax - 2) * block_size) / pa::kTokenQuantum *
+                            pa::kTokenQuantum);
+  int64_t P = round_up(ceil_div(max_len, S), pa::kTokenQuantum);
+  P = std::min(P, p_max);
+  S = ceil_div(max_len, P);
+  if (S > pa::kMaxSplits) {
+    P = round_up(ceil_div(max_len, pa::kMaxSplits), pa::kTokenQuantum);
+    if (P > p_max) return false;  // context too long for this block size
+    S = ceil_div(max_len, P);
+  }
+  *out = {(int)S, (int)P};
+  return true;
+}
+
+// ---------------------------------------------------------------- workspace
+// [0, 256)   device error word (uint32) + padding
+// counters   B*Hkv uint32
+// m, l       B*Hkv*S*G fp32 each        (only when S > 1)
+// acc        B*Hkv*S*G*D fp32            (only when S > 1)
+struct WsLayout {
+  size_t counters, m, l, acc, total;
+};
+
+WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t G, int64_t D, int64_t S) {
+  WsLayout w{};
+  size_t off = 256;
+  w.counters = off;
+  off += align256((size_t)(B * Hkv) * 4);
+  if (S > 1) {
+    const size_t parts = (size_t)(B * Hkv * S * G);
+    w.m = off;
+    off += align256(parts * 4);
+    w.l = off;
+    off += align256(parts * 4);
+    w.acc = off;
+    off += align256(parts * (size_t)D * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Size checks shared by the size query, the plan and the launch.
+pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
+  if (a->B < 0) return PA_ERR_INVALID_ARG;
+  if (a->Hq <= 0 || a->Hkv <= 0 || a->D <= 0) return PA_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (a->Hq / a->Hkv > PA_MAX_GQA_GROUP) return PA_ERR_INVALID_ARG;
+  if (a->D != 128 && a->D != 256) return PA_ERR_UNSUPPORTED;
+  if (a->block_size <= 0 || a->num_blocks <= 0 || a->max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (a->dtype != PA_F16 && a->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (a->splits < 0) return PA_ERR_INVALID_ARG;
+  if (a->B > 65535 || a->Hkv > 65535) return PA_ERR_INVALID_ARG;  // grid limits
+  const int64_t cap = (int64_t)a->max_blocks_per_seq * a->block_size;
+  int64_t ml = a->max_seq_len <= 0 ? cap : a->max_seq_len;
+  if (ml > cap) return PA_ERR_OUT_OF_RANGE;
+  if (ml > INT_MAX) return PA_ERR_OUT_OF_RANGE;
+  *max_len = ml;
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_version(void) { return "0.1.0"; }
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_OUT_OF_RANGE: return "value out of range";
+  }
+  return "unknown status";
+}
+
+pa_status pa_set_device(int device) {
+  if (cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
+                         int* partition_tokens) {
+  if (!a || !splits || !partition_tokens) return PA_ERR_INVALID_ARG;
+  int64_t max_len = 0;
+  const pa_status st = check_sizes(a, &max_len);
+  if (st != PA_OK) return st;
+  if (sm_count <= 0) sm_count = current_sm_count();
+  if (sm_count <= 0) return PA_ERR_CUDA;
+  Plan plan{};
+  if (!make_plan(sm_count, a->B, a->Hkv, a->block_size, max_len, a->splits, &plan))
+    return PA_ERR_UNSUPPORTED;
+  *splits = plan.S;
+  *partition_tokens = plan.P;
+  return PA_OK;
+}
+
+size_t pa_decode_ex_workspace_bytes(const pa_decode_args* a) {
+  int S = 0, P = 0;
+  if (pa_decode_plan(a, 0, &S, &P) != PA_OK) return 0;
+  return ws_layout(a->B, a->Hkv, a->Hq / a->Hkv, a->D, S).total;
+}
+
+size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size,
+                                 int max_seq_len) {
+  pa_decode_args a{};
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.block_size = block_size;
+  a.num_blocks = 1;
+  a.max_blocks_per_seq = max_seq_len > 0 ? (int)ceil_div(max_seq_len, block_size > 0 ? block_size : 1) : 1;
+  a.max_seq_len = max_seq_len;
+  a.dtype = PA_BF16;
+  if (max_seq_len <= 0) return 0;
+  return pa_decode_ex_workspace_bytes(&a);
+}
+
+pa_status pa_workspace_init(void* workspace, size_t bytes, pa_stream_t stream) {
+  if (!workspace) return PA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_read_device_errors(void* workspace, pa_stream_t stream, uint32_t* flags) {
+  if (!workspace || !flags) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(v), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  *flags = v;
+  return PA_OK;
+}
+
+pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
+  if (!a) return PA_ERR_INVALID_ARG;
+  int64_t max_len = 0;
+  pa_status st = check_sizes(a, &max_len);
+  if (st != PA_OK) return st;
+  if (a->B == 0) return PA_OK;  // nothing to compute
+  if (!a->q || !a->k_cache || !a->v_cache || !a->block_tables || !a->seq_lens || !a->out)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->out))
+    return PA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_WORKSPACE;
+
+  const int sm = current_sm_count();
+  if (sm <= 0) return PA_ERR_CUDA;
+  Plan plan{};
+  if (!make_plan(sm, a->B, a->Hkv, a->block_size, max_len, a->splits, &plan))
+    return PA_ERR_UNSUPPORTED;
+  const int G = a->Hq / a->Hkv;
+  const WsLayout w = ws_layout(a->B, a->Hkv, G, a->D, plan.S);
+  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  pa::DecodeParams p{};
+  p.q = a->q;
+  p.k_cache = a->k_cache;
+  p.v_cache = a->v_cache;
+  p.block_tables = a->block_tables;
+  p.seq_lens = a->seq_lens;
+  p.out = a->out;
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(ws + w.counters);
+  p.ws_m = plan.S > 1 ? reinterpret_cast<float*>(ws + w.m) : nullptr;
+  p.ws_l = plan.S > 1 ? reinterpret_cast<float*>(ws + w.l) : nullptr;
+  p.ws_acc = plan.S > 1 ? reinterpret_cast<float*>(ws + w.acc) : nullptr;
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.G = G;
+  p.block_size = a->block_size;
+  p.num_blocks = a->num_blocks;
+  p.max_blocks = a->max_blocks_per_seq;
+  p.max_seq_len = (int)max_len;
+  p.S = plan.S;
+  p.P = plan.P;
+  p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+
+  cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e;
+  const bool bf16 = a->dtype == PA_BF16;
+  if (a->D == 128)
+    e = bf16 ? pa::launch_decode_bf16_d128(p, cs) : pa::launch_decode_f16_d128(p, cs);
+  else
+    e = bf16 ? pa::launch_decode_bf16_d256(p, cs) : pa::launch_decode_f16_d256(p, cs);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, void* out, int B,
+                    int Hq, int Hkv, int D, int block_size, int num_blocks,
+                    int max_blocks_per_seq, int max_seq_len, float scale, pa_dtype dtype,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_decode_args a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.splits = 0;
+  return pa_decode_ex(&a, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Launch parameters shared by the host launcher and the decode kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Tokens staged per CTA are bounded by the block-table slice it keeps in shared
+// memory; split counts are bounded by the merge scratch of the last CTA.
+constexpr int kBtMax = 1024;
+constexpr int kMaxSplits = 1024;
+constexpr int kPartitionMin = 128;  // tokens: below this a split's fixed cost dominates
+constexpr int kTokenQuantum = 32;   // partition sizes are multiples of the warp tile
+
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  void* out;
+  float* ws_m;        // [B*Hkv*S][G]   running max of each split (log2 domain)
+  float* ws_l;        // [B*Hkv*S][G]   softmax denominator of each split
+  float* ws_acc;      // [B*Hkv*S][G][D] unnormalised output of each split
+  uint32_t* counters; // [B*Hkv]        splits finished, reset by the merging CTA
+  uint32_t* err;      // device error word
+  int B, Hq, Hkv, G;
+  int block_size, num_blocks, max_blocks, max_seq_len;
+  int S, P;           // splits and tokens per split
+  float scale_log2;   // scale * log2(e): scores live in the exp2 domain
+};
+
+// One launcher per (dtype, head_dim); each dispatches on the GQA group size.
+cudaError_t launch_decode_bf16_d128(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_bf16_d256(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_f16_d256(const DecodeParams& p, cudaStream_t st);
+
+}  // namespace pa

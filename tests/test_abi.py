@@ -1,0 +1,137 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every symbol
+include/pa.h declares, validates arguments on the host, and plans launches."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_pa_gb300 as pa
+from paged_kv_attention_pa_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return pa.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(pa_[a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), f"libpa.so does not export {n}"
+    assert set(names) == set(pa.SIGNATURES), "binding signatures and header disagree"
+
+
+def test_status_strings_and_version(lib):
+    for code in range(6):
+        assert pa.status_string(code)
+    assert pa.status_string(99) == "unknown status"
+    assert pa.version() == pa.__version__
+
+
+def _args(**kw):
+    a = pa.DecodeArgs()
+    base = dict(q=16, k_cache=32, v_cache=48, block_tables=64, seq_lens=80, out=96,
+                B=1, Hq=8, Hkv=8, D=128, block_size=16, num_blocks=64,
+                max_blocks_per_seq=32, max_seq_len=512, scale=0.088, dtype=pa.PA_BF16, splits=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return a
+
+
+def _call(lib, a, ws=256, nbytes=1 << 20):
+    return lib.pa_decode_ex(ctypes.byref(a), ws, nbytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=12, Hkv=8), pa.PA_ERR_INVALID_ARG),            # Hq % Hkv != 0
+    (dict(Hq=34, Hkv=2), pa.PA_ERR_INVALID_ARG),            # G = 17 > 16
+    (dict(D=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(D=0), pa.PA_ERR_INVALID_ARG),
+    (dict(block_size=0), pa.PA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), pa.PA_ERR_INVALID_ARG),
+    (dict(B=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(splits=-2), pa.PA_ERR_INVALID_ARG),
+    (dict(max_seq_len=513), pa.PA_ERR_OUT_OF_RANGE),        # above 32 blocks * 16
+    (dict(q=0), pa.PA_ERR_INVALID_ARG),
+    (dict(out=0), pa.PA_ERR_INVALID_ARG),
+    (dict(k_cache=40), pa.PA_ERR_INVALID_ARG),              # not 16-byte aligned
+])
+def test_host_validation(lib, kw, code):
+    assert _call(lib, _args(**kw)) == code
+
+
+def test_workspace_checks_precede_cuda(lib):
+    assert _call(lib, _args(), ws=0) == pa.PA_ERR_WORKSPACE
+    assert _call(lib, _args(), ws=272) == pa.PA_ERR_WORKSPACE   # not 256-byte aligned
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _call(lib, _args(B=0, q=0, out=0)) == pa.PA_OK
+
+
+def test_valid_call_without_gpu_reports_cuda(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(lib, _args()) == pa.PA_ERR_CUDA
+
+
+def test_plain_entry_point_validates(lib):
+    rc = lib.pa_decode(16, 32, 48, 64, 80, 96, 1, 12, 8, 128, 16, 64, 32, 512, 0.1,
+                       pa.PA_BF16, 256, 1 << 20, None)
+    assert rc == pa.PA_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ planner
+SM = 152
+
+
+@pytest.mark.parametrize("B,Hkv,bs,L", [
+    (1, 8, 16, 512), (1, 4, 784, 4096), (1, 4, 784, 32768), (1, 8, 16, 1024),
+    (8, 16, 16, 32768), (64, 8, 16, 32768), (1, 1, 1, 300000), (5, 8, 16, 16385),
+    (1, 4, 784, 500), (2, 3, 7, 1000),
+])
+def test_plan_properties(lib, B, Hkv, bs, L):
+    S, P = pa.plan(B, Hkv * 2, Hkv, 128, bs, L, sm_count=SM)
+    assert P % 32 == 0 and P > 0
+    assert S * P >= L, "the splits cover the longest context"
+    assert (S - 1) * P < L, "no split of the longest context is empty"
+    assert S <= 1024
+    assert (P - 1) // bs + 2 <= 1024, "a split's block-table slice fits the CTA buffer"
+    # every SM gets a split unless that would make splits shorter than 128 tokens
+    assert B * Hkv * S >= SM or P <= 160
+
+
+def test_plan_fills_sms_at_batch_one():
+    S, P = pa.plan(1, 24, 4, 256, 784, 32768, sm_count=SM)
+    assert 4 * S >= SM
+    S, P = pa.plan(1, 24, 4, 256, 784, 4096, sm_count=SM)
+    assert 4 * S >= 4096 // 128  # bounded by the minimum split length
+    assert P == 128
+
+
+def test_forced_splits():
+    for want in (1, 2, 3, 7):
+        S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=want, sm_count=SM)
+        assert S == want and S * P >= 1025
+    S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=10000, sm_count=SM)
+    assert P == 32 and S == 33
+
+
+def test_large_batch_needs_no_split():
+    S, P = pa.plan(64, 32, 8, 128, 16, 8192, sm_count=SM)
+    assert S == 1 and P >= 8192

@@ -1,0 +1,315 @@
+"""CUDA path against the float64 oracle, through the C ABI (GB300 only).
+
+Bar: every output finite and rel L-inf <= 1e-2 against the oracle on the
+reference's own max-abs scale ("vLLM's custom ROCm paged-attention kernel wins
+all sixty cells", §1). Small cases compare every output; full-size cases compare
+sampled (sequence, KV head) groups the oracle computes one by one. Inputs are the
+seeded synthetic shapes of the pages' sweeps (§1-§3 of that page; the hybrid
+layer of "Hybrid-SSM decode rate on dual Radeon cards under vLLM").
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import pa_inputs as pi
+from harness import assert_parity, oracle_case, oracle_rows, read_golden
+
+pytestmark = pytest.mark.gpu
+
+GRID_SHAPES = [(8, 8), (16, 8), (24, 8), (32, 8), (32, 16)]
+
+
+def run(pa, case, **kw):
+    c = case if case.q.is_cuda else case.to("cuda")
+    out = pa.decode(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
+                    max_seq_len=kw.pop("max_seq_len", c.max_seq_len), **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def no_device_errors(pa):
+    ws = pa.default_workspace()
+    assert ws is not None
+    assert pa.read_device_errors(ws) == 0
+
+
+def to_np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def check_sampled(pa, case, out, pairs, what):
+    ref = oracle_rows(case, pairs)
+    G = case.Hq // case.Hkv
+    errs = []
+    for (b, kvh), r in ref.items():
+        y = to_np(out[b, kvh * G:(kvh + 1) * G])
+        errs.append(assert_parity(y, r, what=f"{what} b={b} kvh={kvh}"))
+    return max(errs)
+
+
+# ------------------------------------------------------------------ smoke config
+def test_first_config(cuda_lib):
+    # batch 1, 8/8 heads, head_dim 128, block 16, seq 512, 32 blocks of a 64-block cache
+    case = pi.make_case(1, 8, 8, 128, 16, [512], seed=0, num_blocks=64)
+    y = run(cuda_lib, case)
+    err = assert_parity(to_np(y), oracle_case(case), what="first config")
+    assert err < 5e-3
+    no_device_errors(cuda_lib)
+
+
+def test_plain_and_ex_entry_points_agree(cuda_lib):
+    case = pi.make_case(2, 16, 8, 128, 16, [700, 1500], seed=1).to("cuda")
+    a = run(cuda_lib, case)
+    b = cuda_lib.decode_plain(case.q, case.k_cache, case.v_cache, case.block_tables,
+                              case.seq_lens, case.scale, max_seq_len=case.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ GQA x depth grid
+@pytest.mark.parametrize("hq,hkv", GRID_SHAPES)
+@pytest.mark.parametrize("B", [1, 8])
+def test_grid_small_full_compare(cuda_lib, hq, hkv, B):
+    # every output compared, at depths the oracle finishes quickly
+    for L in (1024, 2048):
+        case = pi.make_case(B, hq, hkv, 128, 16, [L] * B, seed=L + B)
+        y = run(cuda_lib, case)
+        assert_parity(to_np(y), oracle_case(case), what=f"grid {hq}/{hkv} B={B} L={L}")
+    no_device_errors(cuda_lib)
+
+
+@pytest.mark.parametrize("hq,hkv", GRID_SHAPES)
+def test_grid_full_depths_sampled(cuda_lib, hq, hkv):
+    rng = random.Random(hq * 100 + hkv)
+    for B in (1, 8):
+        for L in (4096, 8192, 16384, 32768):
+            case = pi.make_case(B, hq, hkv, 128, 16, [L] * B, seed=7, device="cuda")
+            y = run(cuda_lib, case)
+            pairs = {(rng.randrange(B), rng.randrange(hkv)) for _ in range(3)}
+            check_sampled(cuda_lib, case, y, sorted(pairs), f"grid {hq}/{hkv} B={B} L={L}")
+            assert torch.isfinite(y).all()
+            del case, y
+    no_device_errors(cuda_lib)
+
+
+# ------------------------------------------------------------------ tail straddle
+TAIL_LENS = [1023, 1025, 4095, 4097, 16385, 1024, 4096]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8)])
+@pytest.mark.parametrize("L", TAIL_LENS)
+def test_tail_poison_matrix(cuda_lib, dtype, hq, hkv, L):
+    outs = {}
+    for mode in pi.POISON_MODES:
+        case = pi.make_case(1, hq, hkv, 128, 16, [L], dtype=dtype, seed=3, poison=mode)
+        y = run(cuda_lib, case)
+        if mode == "none":
+            ref = oracle_case(case)
+        assert_parity(to_np(y), ref, what=f"tail {mode} L={L} {dtype} {hq}/{hkv}")
+        outs[mode] = y
+    # the fill of the empty slots must not change a single bit of the output
+    for mode, y in outs.items():
+        assert torch.equal(y, outs["none"]), f"output depends on the {mode} fill"
+    no_device_errors(cuda_lib)
+
+
+def test_tail_batch_of_all_lengths(cuda_lib):
+    lens = [1023, 1025, 4095, 4097, 16385]
+    for mode in ("v_nan", "kv_nan", "kv_1e4"):
+        case = pi.make_case(5, 32, 8, 128, 16, lens, seed=4, poison=mode)
+        y = run(cuda_lib, case)
+        assert_parity(to_np(y), oracle_case(case), what=f"tail batch {mode}")
+
+
+def test_poison_pattern_golden_on_gpu(cuda_lib):
+    # The patched column of the pages' Figure 4: no mode poisons at any length.
+    for mode, kind, stock, patched in read_golden("poison_pattern.txt"):
+        L = 4090 if kind == "straddle" else 4096
+        case = pi.make_case(1, 16, 8, 128, 16, [L], seed=5, poison=mode)
+        y = run(cuda_lib, case)
+        poisoned = (not torch.isfinite(y).all().item())
+        assert int(poisoned) == int(patched) == 0
+
+
+# ------------------------------------------------------------------ hybrid layer
+@pytest.mark.parametrize("L", [500, 1000, 2048, 4096, 8192, 12288, 16384, 20480, 24576,
+                               28672, 32768])
+def test_hybrid_layer(cuda_lib, L):
+    # 24 query / 4 KV heads (ratio 6), head_dim 256, block 784 (non power of two)
+    case = pi.make_case(1, 24, 4, 256, 784, [L], seed=L)
+    y = run(cuda_lib, case)
+    assert_parity(to_np(y), oracle_case(case), what=f"hybrid L={L}")
+    no_device_errors(cuda_lib)
+
+
+def test_hybrid_nan_spare(cuda_lib):
+    case = pi.make_case(1, 24, 4, 256, 784, [5000], seed=8, poison="kv_nan")
+    ref = oracle_case(case)
+    y = run(cuda_lib, case)
+    assert_parity(to_np(y), ref, what="hybrid nan spare")
+    z = run(cuda_lib, pi.make_case(1, 24, 4, 256, 784, [5000], seed=8, poison="none"))
+    assert torch.equal(y, z)
+
+
+# ------------------------------------------------------------------ mixed serving batch
+def test_mixed_serving_batch(cuda_lib):
+    lens = pi.uniform_seq_lens(64, 1024, 32768, seed=0)
+    case = pi.make_case(64, 32, 8, 128, 16, lens, seed=0, pool_factor=1.1, poison="kv_nan",
+                        device="cuda")
+    y = run(cuda_lib, case)
+    assert torch.isfinite(y).all()
+    rng = random.Random(0)
+    pairs = sorted({(rng.randrange(64), rng.randrange(8)) for _ in range(12)} |
+                   {(int(np.argmax(lens)), 0), (int(np.argmin(lens)), 7)})
+    check_sampled(cuda_lib, case, y, pairs, "mixed batch")
+    no_device_errors(cuda_lib)
+
+
+# ------------------------------------------------------------------ splits
+@pytest.mark.parametrize("L", [1025, 4097])
+def test_split_sweep(cuda_lib, L):
+    case = pi.make_case(2, 24, 8, 128, 16, [L, L // 3], seed=9).to("cuda")
+    ref = oracle_case(case)
+    results = {}
+    for S in (1, 2, 3, 7, 10000):
+        y = run(cuda_lib, case, splits=S)
+        assert_parity(to_np(y), ref, what=f"splits={S} L={L}")
+        y2 = run(cuda_lib, case, splits=S)
+        assert torch.equal(y, y2), "equal splits must give bit-identical results"
+        results[S] = y
+    no_device_errors(cuda_lib)
+
+
+def test_split_sweep_head256(cuda_lib):
+    case = pi.make_case(1, 24, 4, 256, 784, [3000], seed=10).to("cuda")
+    ref = oracle_case(case)
+    for S in (1, 2, 5, 94):
+        assert_parity(to_np(run(cuda_lib, case, splits=S)), ref, what=f"d256 splits={S}")
+
+
+# ------------------------------------------------------------------ invariances
+def test_block_permutation_invariance(cuda_lib):
+    case = pi.make_case(3, 32, 8, 128, 16, [3001, 17, 4096], seed=11, poison="kv_nan")
+    y1 = run(cuda_lib, case)
+    y2 = run(cuda_lib, pi.repage(case, seed=12))
+    assert torch.equal(y1, y2), "the block table layout must not change a bit"
+    case = pi.make_case(1, 24, 4, 256, 784, [6000], seed=13)
+    assert torch.equal(run(cuda_lib, case), run(cuda_lib, pi.repage(case, seed=14)))
+
+
+def test_equal_scores_give_mean_of_v(cuda_lib):
+    case = pi.make_case(1, 16, 8, 128, 16, [777], seed=15).to("cuda")
+    case.q.zero_()
+    y = to_np(run(cuda_lib, case))
+    G = 2
+    for h in range(16):
+        mean = pi.to_f64_numpy(case.V[0][:, h // G, :]).mean(axis=0)
+        assert np.abs(y[0, h] - mean).max() <= 1e-2 * np.abs(mean).max()
+
+
+def test_one_hot_score_selects_row(cuda_lib):
+    # K[t0] = c * q / |q|^2 per head with scale*c = 50, every other live K row zero:
+    # softmax puts weight 1 - O(300 e^-50) on token t0, so out = V[t0].
+    case = pi.make_case(1, 8, 8, 128, 16, [300], seed=16, dtype="f16")
+    t0 = 123
+    q = case.q[0].double()
+    K = torch.zeros_like(case.K[0])
+    for h in range(8):
+        K[t0, h] = (50.0 / case.scale * q[h] / (q[h] @ q[h])).to(K.dtype)
+    case.K[0].copy_(K)
+    bt = case.block_tables[0].long()
+    t = torch.arange(300)
+    case.k_cache[bt[t // 16], t % 16] = case.K[0]
+    y = to_np(run(cuda_lib, case))
+    v = pi.to_f64_numpy(case.V[0][t0])
+    assert np.abs(y[0] - v).max() <= 1e-2 * np.abs(v).max()
+
+
+# ------------------------------------------------------------------ edge cases
+def test_edge_lengths(cuda_lib):
+    case = pi.make_case(6, 16, 8, 128, 16, [0, 1, 15, 16, 17, 0], seed=17, poison="kv_nan",
+                        table_fill="oob")
+    y = run(cuda_lib, case)
+    assert torch.all(y[0] == 0) and torch.all(y[5] == 0)
+    assert_parity(to_np(y), oracle_case(case), what="edge lengths")
+    no_device_errors(cuda_lib)
+
+
+def test_all_empty_batch(cuda_lib):
+    case = pi.make_case(3, 8, 8, 128, 16, [0, 0, 0], seed=18)
+    c = case.to("cuda")
+    out = torch.full_like(c.q, float("nan"))
+    cuda_lib.decode(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
+                    out=out, max_seq_len=16)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("hq,hkv,D,bs,dtype", [
+    (5, 1, 128, 16, "bf16"), (7, 1, 256, 16, "f16"), (16, 1, 128, 32, "bf16"),
+    (12, 1, 256, 784, "bf16"), (32, 2, 128, 16, "f16"), (3, 3, 256, 48, "bf16"),
+    (64, 64, 128, 16, "bf16"),
+])
+def test_other_shapes(cuda_lib, hq, hkv, D, bs, dtype):
+    case = pi.make_case(2, hq, hkv, D, bs, [999, 2500], dtype=dtype, seed=19)
+    assert_parity(to_np(run(cuda_lib, case)), oracle_case(case),
+                  what=f"{hq}/{hkv} D={D} bs={bs} {dtype}")
+
+
+def test_determinism(cuda_lib):
+    case = pi.make_case(4, 24, 8, 128, 16, [5000, 300, 2048, 7777], seed=20).to("cuda")
+    a = run(cuda_lib, case)
+    b = run(cuda_lib, case)
+    assert torch.equal(a, b)
+
+
+def test_cuda_graph_replay(cuda_lib):
+    case = pi.make_case(2, 32, 8, 128, 16, [4000, 2500], seed=21).to("cuda")
+    ref = run(cuda_lib, case)
+    out = torch.empty_like(case.q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run_kw = dict(out=out, max_seq_len=case.max_seq_len)
+        cuda_lib.decode(case.q, case.k_cache, case.v_cache, case.block_tables, case.seq_lens,
+                        case.scale, **run_kw)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            cuda_lib.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                            case.seq_lens, case.scale, **run_kw)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+# ------------------------------------------------------------------ device-side errors
+def test_bad_block_index_is_reported_not_faulted(cuda_lib):
+    case = pi.make_case(1, 8, 8, 128, 16, [100], seed=22).to("cuda")
+    case.block_tables[0, 2] = case.num_blocks + 5     # a live token's block
+    y = run(cuda_lib, case)
+    assert torch.isfinite(y).all()
+    assert cuda_lib.read_device_errors(cuda_lib.default_workspace()) == cuda_lib.PA_DEVERR_BLOCK_INDEX
+    case.block_tables[0, 2] = -3
+    run(cuda_lib, case)
+    assert cuda_lib.read_device_errors(cuda_lib.default_workspace()) == cuda_lib.PA_DEVERR_BLOCK_INDEX
+
+
+def test_seq_len_above_bound_is_reported(cuda_lib):
+    case = pi.make_case(1, 8, 8, 128, 16, [100], seed=23).to("cuda")
+    y = run(cuda_lib, case, max_seq_len=64)          # host bound smaller than the real length
+    assert torch.isfinite(y).all()
+    assert cuda_lib.read_device_errors(cuda_lib.default_workspace()) == cuda_lib.PA_DEVERR_SEQ_LEN
+
+
+def test_host_errors_raise(cuda_lib):
+    case = pi.make_case(1, 8, 8, 128, 16, [100], seed=24).to("cuda")
+    with pytest.raises(cuda_lib.PAError):
+        cuda_lib.decode(case.q, case.k_cache, case.v_cache, case.block_tables, case.seq_lens,
+                        case.scale, max_seq_len=10 ** 6)
+    with pytest.raises(ValueError):
+        cuda_lib.decode(case.q.cpu(), case.k_cache, case.v_cache, case.block_tables,
+                        case.seq_lens, case.scale)
