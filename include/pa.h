@@ -34,7 +34,7 @@
  *    q, k_cache, v_cache and out must be 16-byte aligned.
  *  - Device-side problems (a block table entry outside [0, num_blocks) for a live
  *    token, a seq_len that is negative or above max_seq_len or above
- *    max_blocks_per_seq*block_size, a pipeline wait that gave up) never fault:
+ *    max_blocks_per_seq*block_size) never fault:
  *    the kernel clamps, keeps going, and ORs a PA_DEVERR_* bit into the workspace
  *    header; read it with pa_read_device_errors. The output of such a call is
  *    finite but not meaningful.
@@ -63,7 +63,7 @@ typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 /* Bits of the device error word (workspace header). */
 #define PA_DEVERR_BLOCK_INDEX 1u /* a live token's block table entry was outside [0, num_blocks) */
 #define PA_DEVERR_SEQ_LEN 2u     /* a seq_len < 0, > max_seq_len or > max_blocks_per_seq*block_size */
-#define PA_DEVERR_TIMEOUT 4u     /* a shared-memory pipeline wait gave up (bounded spin) */
+#define PA_DEVERR_TIMEOUT 4u     /* reserved: a bounded wait gave up (no kernel spins today) */
 
 typedef void* pa_stream_t; /* cudaStream_t */
 
@@ -92,12 +92,12 @@ typedef struct pa_decode_args {
 
 /*
  * Workspace bytes pa_decode needs for these sizes on the current device. The
- * workspace holds the device error word, one counter per (sequence, KV head) and
- * the fp32 split partials (m, l, acc). It must be zero-filled once before its first
- * use (pa_workspace_init or any memset); every call leaves it ready for the next.
- * Calls that overlap on the GPU must not share a workspace. max_seq_len <= 0 means
- * max_blocks_per_seq * block_size is not known here: pass the real bound.
- * Returns 0 for invalid sizes.
+ * workspace holds the device error word (first 4 bytes, which must be zero
+ * before the first call: pa_workspace_init or any memset) and the fp32 split
+ * partials (m, l, acc), which every call writes before it reads them. One
+ * workspace serves calls of any shape that fit its size; calls that overlap on
+ * the GPU must not share one. Returns 0 for invalid sizes (max_seq_len must be
+ * > 0 here).
  */
 size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size, int max_seq_len);
 
@@ -123,7 +123,7 @@ size_t pa_decode_ex_workspace_bytes(const pa_decode_args* args);
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D))
  *   dtype         PA_F16 or PA_BF16 for q, caches and out
  *   workspace     device scratch of >= pa_decode_workspace_bytes(...) bytes,
- *                 256-byte aligned, zero-filled before first use
+ *                 256-byte aligned, its first 4 bytes zero before first use
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE,
  * PA_ERR_OUT_OF_RANGE (max_seq_len above capacity), PA_ERR_CUDA.
  */
@@ -139,7 +139,7 @@ pa_status pa_decode_ex(const pa_decode_args* args, void* workspace, size_t works
 
 /*
  * The launch plan pa_decode_ex would use on a GPU with `sm_count` SMs: the number
- * of context splits and the tokens per split (a multiple of 32). Pure host
+ * of context splits and the tokens per split (a multiple of 16). Pure host
  * arithmetic; needs no GPU. sm_count <= 0 means the current device's SM count.
  */
 pa_status pa_decode_plan(const pa_decode_args* args, int sm_count, int* splits,

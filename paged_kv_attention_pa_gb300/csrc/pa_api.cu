@@ -19,39 +19,22 @@ inline int64_t round_up(int64_t a, int64_t q) { return ceil_div(a, q) * q; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------- split plan
-// Choose S (splits of each sequence's context) and P (tokens per split).
-// The unit of parallel work is a (sequence, KV head, split). With one resident
-// CTA per SM, S is chosen so that B * Hkv * S covers every SM, but no split gets
-// fewer than kPartitionMin tokens. P is a multiple of the 32-token warp tile and
-// small enough that a split's block-table slice fits the CTA's staging buffer.
+// Choose S (splits of each sequence's context) and P (tokens per split, a
+// multiple of the 16-token warp tile). The unit of parallel work is a (sequence,
+// KV head, split) CTA, one resident per SM. The cost of a plan is the number of
+// CTA waves times the tokens a CTA streams plus its fixed cost; candidates are
+// one split and the largest split counts that fill exactly 1..4 waves. P is also
+// bounded so that a split's block-table slice fits the CTA's staging buffer.
 struct Plan {
   int S;
   int P;
 };
 
-bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t max_len,
-               int requested, Plan* out) {
-  if (max_len <= 0) {
-    *out = {1, pa::kTokenQuantum};
-    return true;
-  }
-  const int64_t units = B * Hkv;
-  int64_t S;
-  if (requested > 0) {
-    S = requested;
-  } else {
-    S = ceil_div(sm_count > 0 ? sm_count : 1, units);
-    S = std::min<int64_t>(S, ceil_div(max_len, pa::kPartitionMin));
-    S = std::max<int64_t>(S, 1);
-  }
-  S = std::min<int64_t>(S, ceil_div(max_len, pa::kTokenQuantum));
-  const int64_t p_max =
-      std::max<int64_t>(pa::kTokenQuantum,
-                        ((int64_t)(pa::kBtMax - 2) * block_size) / pa::kTokenQuantum *
-                            pa::kTokenQuantum);
-  int64_t P = round_up(ceil_div(max_len, S), pa::kTokenQuantum);
+bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, Plan* out) {
+  int64_t P = round_up(ceil_div(max_len, std::max<int64_t>(S_req, 1)), pa::kTokenQuantum);
+  if (floor_p) P = std::max<int64_t>(P, pa::kPartitionMin);
   P = std::min(P, p_max);
-  S = ceil_div(max_len, P);
+  int64_t S = ceil_div(max_len, P);
   if (S > pa::kMaxSplits) {
     P = round_up(ceil_div(max_len, pa::kMaxSplits), pa::kTokenQuantum);
     if (P > p_max) return false;  // context too long for this block size
@@ -61,20 +44,49 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t
   return true;
 }
 
+bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t max_len,
+               int requested, Plan* out) {
+  if (max_len <= 0) {
+    *out = {1, pa::kTokenQuantum};
+    return true;
+  }
+  const int64_t units = B * Hkv;
+  const int64_t sm = sm_count > 0 ? sm_count : 1;
+  const int64_t p_max =
+      std::max<int64_t>(pa::kTokenQuantum,
+                        ((int64_t)(pa::kBtMax - 2) * block_size) / pa::kTokenQuantum *
+                            pa::kTokenQuantum);
+  if (requested > 0) return plan_for(requested, max_len, p_max, false, out);
+  bool found = false;
+  int64_t best_cost = 0;
+  const int64_t cands[6] = {1, sm / units, 2 * sm / units, 3 * sm / units, 4 * sm / units,
+                            ceil_div(sm, units)};
+  for (int64_t c : cands) {
+    if (c < 1) continue;
+    Plan pl{};
+    if (!plan_for(c, max_len, p_max, true, &pl)) continue;
+    const int64_t waves = ceil_div(units * pl.S, sm);
+    const int64_t cost = waves * (pl.P + pa::kSplitOverhead);
+    if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
+      *out = pl;
+      best_cost = cost;
+      found = true;
+    }
+  }
+  return found;
+}
+
 // ---------------------------------------------------------------- workspace
 // [0, 256)   device error word (uint32) + padding
-// counters   B*Hkv uint32
 // m, l       B*Hkv*S*G fp32 each        (only when S > 1)
-// acc        B*Hkv*S*G*D fp32            (only when S > 1)
+// acc        B*Hkv*S*G*D fp32           (only when S > 1)
 struct WsLayout {
-  size_t counters, m, l, acc, total;
+  size_t m, l, acc, total;
 };
 
 WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t G, int64_t D, int64_t S) {
   WsLayout w{};
   size_t off = 256;
-  w.counters = off;
-  off += align256((size_t)(B * Hkv) * 4);
   if (S > 1) {
     const size_t parts = (size_t)(B * Hkv * S * G);
     w.m = off;
@@ -117,6 +129,8 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   if (a->dtype != PA_F16 && a->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (a->splits < 0) return PA_ERR_INVALID_ARG;
   if (a->B > 65535 || a->Hkv > 65535) return PA_ERR_INVALID_ARG;  // grid limits
+  // kernels address cache rows with 32-bit row indices
+  if ((int64_t)a->num_blocks * a->block_size * a->Hkv > (int64_t)UINT32_MAX) return PA_ERR_UNSUPPORTED;
   const int64_t cap = (int64_t)a->max_blocks_per_seq * a->block_size;
   int64_t ml = a->max_seq_len <= 0 ? cap : a->max_seq_len;
   if (ml > cap) return PA_ERR_OUT_OF_RANGE;
@@ -245,7 +259,6 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.seq_lens = a->seq_lens;
   p.out = a->out;
   p.err = reinterpret_cast<uint32_t*>(ws);
-  p.counters = reinterpret_cast<uint32_t*>(ws + w.counters);
   p.ws_m = plan.S > 1 ? reinterpret_cast<float*>(ws + w.m) : nullptr;
   p.ws_l = plan.S > 1 ? reinterpret_cast<float*>(ws + w.l) : nullptr;
   p.ws_acc = plan.S > 1 ? reinterpret_cast<float*>(ws + w.acc) : nullptr;

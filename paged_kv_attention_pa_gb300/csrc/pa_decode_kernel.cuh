@@ -6,26 +6,27 @@
 // split-KV fix of the same page so that B * Hkv * splits fills every SM even at
 // batch 1 with 4 KV heads).
 //
-// Warp roles inside a CTA:
-//   warp NW (producer)  stages the CTA's block-table slice, then streams K/V
-//                       rows into a ring of shared-memory stages with 1-D bulk
-//                       copies (TMA engine, one row of D elements each), each
-//                       stage completing on an mbarrier as transaction bytes.
-//                       Only rows of live tokens (t < seq_len) are copied: the
-//                       unwritten tail of the last block is never read
-//                       ("vLLM's custom ROCm paged-attention kernel wins all
-//                       sixty cells", §5, the V-load fault).
-//   warps 0..NW-1       consume warp tiles round-robin. Scores: lane-per-token,
-//   (consumers)         q broadcast from shared memory, packed fp32x2 FMAs,
-//                       tokens past seq_len set to -inf by select. Online
-//                       softmax in the exp2 domain with warp-shuffle maxima.
-//                       PV: lane-per-output-element, p broadcast from shared
-//                       memory; the loop stops at the last live token, so V rows
-//                       past seq_len never reach the accumulator.
-// Epilogue: the consumer warps merge their (m, l, acc) in shared memory. A single
-// split writes the output; otherwise the split's partial goes to the workspace
-// and the last CTA of the (sequence, KV head) to finish (atomic counter, no
-// waiting) merges all partials and writes the output.
+// Loads. Every warp streams its own 16-token tiles (tile j goes to warp j % NW)
+// through a private ring of DEPTH shared-memory slots with 16-byte cp.async
+// copies (L2 evict-first), DEPTH - 1 tiles in flight while it computes one: per
+// warp pipelines keep ~140-170 KB of loads in flight per SM. Only rows of live
+// tokens (t < seq_len) are copied; the unwritten tail of the last block is never
+// read ("vLLM's custom ROCm paged-attention kernel wins all sixty cells", §5,
+// the V-load fault), and V rows of a partial tile are zeroed in shared memory so
+// that the tensor-core sum over tokens only ever sees finite values there.
+//
+// Math. The GQA group's two contractions run on tensor cores per warp
+// (mma.sync m16n8k16, fp32 accumulate): S^T[16 tokens x 8 heads] = K_tile q^T,
+// then O^T[d x 8 heads] += V_tile^T P^T with P rounded to the input type. Scores
+// of tokens past seq_len become -inf by select before the online softmax (exp2
+// domain, running max and sum per head). Groups of 9..16 heads use two 8-head
+// column tiles.
+//
+// Epilogue: the warps merge their (m, l, acc) in shared memory. A sequence that
+// fits in one split gets its output written here; otherwise the split's partial
+// goes to the workspace and merge_kernel, chained behind this grid with a
+// programmatic dependent launch, combines the splits of every (sequence, head)
+// in parallel.
 #pragma once
 
 #include <cstdint>
@@ -34,61 +35,79 @@
 #include "pa_device.cuh"
 #include "pa_params.h"
 
+#ifndef PA_WARPS_D128
+#define PA_WARPS_D128 4
+#endif
+#ifndef PA_WARPS_D256
+#define PA_WARPS_D256 4
+#endif
+
 namespace pa {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kSmemBudget = 220 * 1024;
-constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s: only a logic error gets here
-constexpr int kMergeBar = 1;                           // named barrier id for consumers
+constexpr int kSmemBudget = 224 * 1024;
+constexpr int kTileTokens = 16;  // M of the score MMA
 
-template <int D, int GT>
+template <int D, int NT>
 struct Cfg {
-  static constexpr int LPT = D / 128;           // lanes per token in the score phase
-  static constexpr int TW = 32 / LPT;           // tokens per warp tile
+  static constexpr int NW = D == 128 ? PA_WARPS_D128 : PA_WARPS_D256;  // warps per CTA
+  static constexpr int THREADS = NW * 32;
+  static constexpr int TW = kTileTokens;
+  static constexpr int GT = 8 * NT;             // heads computed (G padded)
   static constexpr int ROWB = D * 2 + 16;       // smem row pitch, padded against bank conflicts
-  static constexpr int TILE_BYTES = TW * ROWB;  // K (or V) half of a stage
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int DPL = D / 32;            // output elements per lane in the PV phase
-  static constexpr int GP = (GT + 3) / 4 * 4;   // pitch of a token's p row (floats)
-  static constexpr int QH = D / LPT;            // q elements a lane's score covers
-  static constexpr int QROW = QH + 4;           // padded q half-row (floats)
-  static constexpr int CHAINS = GT <= 4 ? 2 : 1;  // independent FMA chains per head
-  static constexpr int Q_BYTES = GT * LPT * QROW * 4;
-  static constexpr int P_BYTES = kConsumerWarps * TW * GP * 4;
+  static constexpr int CPR = D * 2 / 16;        // 16-byte chunks per row
+  static constexpr int TILE_BYTES = TW * ROWB;  // K (or V) half of a slot
+  static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
+  static constexpr int KS = D / 16;             // k-steps of the score MMA = d-blocks of PV
+  static constexpr int COPIES = TW * CPR / 32;  // 16-byte copies per lane per operand per tile
   static constexpr int BT_BYTES = kBtMax * 4;
-  static constexpr int FIXED = Q_BYTES + P_BYTES + BT_BYTES + 512;
-  static constexpr int NS_FIT = (kSmemBudget - FIXED) / STAGE_BYTES;
-  static constexpr int NS = NS_FIT > 12 ? 12 : NS_FIT;
-  static constexpr int SMEM = NS * STAGE_BYTES + FIXED;
-  static constexpr int RING = NS * STAGE_BYTES;
-  static_assert(NS >= 2 * kConsumerWarps, "need at least two stages per consumer warp");
-  static_assert(kConsumerWarps * GT * (D + 2) * 4 <= RING, "CTA merge must fit in the ring");
-  static_assert((kMaxSplits + 2) * GT * 4 <= RING, "split merge must fit in the ring");
+  static constexpr int FIXED = BT_BYTES + 256;
+  static constexpr int DEPTH_FIT = (kSmemBudget - FIXED) / (NW * SLOT_BYTES);
+  static constexpr int DEPTH = DEPTH_FIT > 12 ? 12 : DEPTH_FIT;  // slots per warp
+  static constexpr int RING = NW * DEPTH * SLOT_BYTES;
+  static constexpr int SMEM = RING + FIXED;
+  static_assert((TW * CPR) % 32 == 0, "tile shape");
+  static_assert(DEPTH >= 2, "need at least two slots per warp");
+  static_assert(NW * GT * (D + 2) * 4 <= RING, "CTA merge must fit in the ring");
 };
 
-template <typename T, int D, int GT>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  using C = Cfg<D, GT>;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const DecodeParams p) {
+  using C = Cfg<D, NT>;
+  constexpr int GT = C::GT;
+  constexpr int kWarps = C::NW;
+  constexpr int kThreads = C::THREADS;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* q_s = reinterpret_cast<float*>(smem + C::RING);
-  float* p_s = reinterpret_cast<float*>(smem + C::RING + C::Q_BYTES);
-  int* bt_s = reinterpret_cast<int*>(smem + C::RING + C::Q_BYTES + C::P_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::Q_BYTES + C::P_BYTES +
-                                               C::BT_BYTES);
-  uint64_t* empty = full + C::NS;
-  int* flag_s = reinterpret_cast<int*>(empty + C::NS);
+  int* bt_s = reinterpret_cast<int*>(smem + C::RING);
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2;  // fragment row group
+  const int tig = lane & 3;   // thread in group
   const int G = p.G;
   T* out = reinterpret_cast<T*>(p.out);
   const size_t head0 = (size_t)b * p.Hq + (size_t)kvh * G;
+
+  // Inputs may come from the previous kernel in the stream: wait for it (a no-op
+  // without a programmatic launch), then let the merge grid get scheduled.
+  pdl_wait();
+  pdl_launch_dependents();
 
   // ---- context length, validated against the bounds the launch was planned for
   int L = __ldg(p.seq_lens + b);
@@ -111,25 +130,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
   const int n_splits = (L + p.P - 1) / p.P;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    fence_barrier_init();
+  // ---- this split's block-table slice, validated
+  const int blk0 = t_begin / p.block_size;
+  int nb = (t_end - 1) / p.block_size - blk0 + 1;
+  if (nb > kBtMax) {  // the planner never allows this; stay in bounds regardless
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
+    nb = kBtMax;
   }
-  __syncthreads();
-
-  if (warp == kConsumerWarps) {
-    // ================================================================ producer
-    const int blk0 = t_begin / p.block_size;
-    int nb = (t_end - 1) / p.block_size - blk0 + 1;
-    if (nb > kBtMax) {  // the planner never allows this; stay in bounds regardless
-      if (lane == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
-      nb = kBtMax;
-    }
+  {
     const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks;
-    for (int i = lane; i < nb; i += 32) {
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
       int phys = __ldg(bt_row + blk0 + i);
       if (phys < 0 || phys >= p.num_blocks) {
         atomicOr(p.err, PA_DEVERR_BLOCK_INDEX);
@@ -137,212 +147,205 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
       bt_s[i] = phys;
     }
-    __syncwarp();
-    const uint64_t pol = l2_evict_first_policy();
-    const T* kbase = reinterpret_cast<const T*>(p.k_cache);
-    const T* vbase = reinterpret_cast<const T*>(p.v_cache);
-    int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % C::NS;
-      const uint32_t par = ((j / C::NS) & 1) ^ 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&empty[s], par, kWaitLimitCycles);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
-        break;
+  }
+  // ---- query fragments (B operand of the score MMA), unscaled, zero for padded heads
+  uint32_t qf[NT][C::KS][2];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + gid;
+      const bool ok = g < G;
+      const size_t rowp = ((head0 + (ok ? g : 0)) * D) / 2;  // in bf16/f16 pairs
+#pragma unroll
+      for (int kk = 0; kk < C::KS; ++kk) {
+        qf[nt][kk][0] = ok ? __ldg(q32 + rowp + kk * 8 + tig) : 0u;
+        qf[nt][kk][1] = ok ? __ldg(q32 + rowp + kk * 8 + 4 + tig) : 0u;
       }
+    }
+  }
+  __syncthreads();
+
+  // ---- per-warp copy pipeline
+  const uint64_t pol = l2_evict_first_policy();
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
+  const ptrdiff_t v_minus_k =
+      reinterpret_cast<const uint8_t*>(p.v_cache) - reinterpret_cast<const uint8_t*>(p.k_cache);
+  uint8_t* my_ring = ring + warp * C::DEPTH * C::SLOT_BYTES;
+  const uint32_t my_ring_s = smem_addr(my_ring);
+  const int my_tiles = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+
+  // Issue the copies of this warp's k-th tile (a commit group even when empty).
+  auto issue = [&](int k) {
+    if (k < my_tiles) {
+      const int j = warp + k * kWarps;
       const int t0 = t_begin + j * C::TW;
       const int nv = min(C::TW, t_end - t0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nv * 2 * D * sizeof(T)));
-      __syncwarp();
+      // lanes 0..TW-1 resolve one row each: cache row index of token t0 + lane
+      uint32_t ridx = 0;
       if (lane < nv) {
         const int t = t0 + lane;
         const int lb = t / p.block_size;
         const int off = t - lb * p.block_size;
-        const int idx = min(lb - blk0, nb - 1);
-        const size_t row = ((size_t)bt_s[idx] * p.block_size + off) * p.Hkv + kvh;
-        uint8_t* dk = ring + s * C::STAGE_BYTES + lane * C::ROWB;
-        bulk_g2s(dk, kbase + row * D, D * sizeof(T), &full[s], pol);
-        bulk_g2s(dk + C::TILE_BYTES, vbase + row * D, D * sizeof(T), &full[s], pol);
+        const int phys = bt_s[min(lb - blk0, nb - 1)];
+        ridx = ((uint32_t)phys * (uint32_t)p.block_size + (uint32_t)off) * (uint32_t)p.Hkv +
+               (uint32_t)kvh;
       }
-      issued = j + 1;
-    }
-    // Do not leave while copies into this CTA's shared memory may be in flight.
-    if (lane == 0) {
-      const int first = issued > C::NS ? issued - C::NS : 0;
-      for (int j = first; j < issued; ++j)
-        if (!mbar_wait_bounded(&full[j % C::NS], (j / C::NS) & 1, kWaitLimitCycles)) {
-          atomicOr(p.err, PA_DEVERR_TIMEOUT);
-          break;
+      const uint32_t slot = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
+#pragma unroll
+      for (int i = 0; i < C::COPIES; ++i) {
+        const int flat = i * 32 + lane;
+        const int r = flat / C::CPR, c = flat % C::CPR;
+        const uint32_t rr = __shfl_sync(0xffffffffu, ridx, r);
+        if (r < nv) {
+          const uint8_t* src = kbase + (size_t)rr * (D * 2) + c * 16;
+          const uint32_t dst = slot + r * C::ROWB + c * 16;
+          cp_async16(dst, src, pol);
+          cp_async16(dst + C::TILE_BYTES, src + v_minus_k, pol);
         }
+      }
     }
-    return;
-  }
+    cp_async_commit();
+  };
 
-  // ================================================================== consumers
-  const int ctid = threadIdx.x;  // 0 .. kConsumerThreads-1
-  {
-    const T* qg = reinterpret_cast<const T*>(p.q) + head0 * D;
-    for (int i = ctid; i < GT * D; i += kConsumerThreads) {
-      const int g = i / D, d = i - (i / D) * D;
-      const float v = g < G ? to_f32<T>(qg[(size_t)g * D + d]) * p.scale_log2 : 0.f;
-      const int hf = d / C::QH, dd = d - hf * C::QH;
-      q_s[(g * C::LPT + hf) * C::QROW + dd] = v;
-    }
-  }
-  named_bar_sync(kMergeBar, kConsumerThreads);
-
-  const int r = lane % C::TW;   // token of the warp tile this lane scores
-  const int hf = lane / C::TW;  // which half of D (head_dim 256 only)
-  float m[GT], l[GT];
-  float2 acc[GT][C::DPL / 2];
 #pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int i = 0; i < C::DPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
-  }
-  float* pw = p_s + warp * C::TW * C::GP;
+  for (int k = 0; k < C::DEPTH - 1; ++k) issue(k);
 
-  for (int j = warp; j < n_tiles; j += kConsumerWarps) {
-    const int s = j % C::NS;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(&full[s], (j / C::NS) & 1, kWaitLimitCycles);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-      if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
-      break;
-    }
+  // running state: this thread's heads are nt*8 + 2*tig + {0, 1}
+  float m[NT][2], l[NT][2];
+  float o[NT][C::KS][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = -INFINITY;
+    l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+    for (int dd = 0; dd < C::KS; ++dd) o[nt][dd][0] = o[nt][dd][1] = o[nt][dd][2] = o[nt][dd][3] = 0.f;
+  }
+  // ldmatrix row addresses (byte offsets inside a tile) for this lane
+  const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB + (lane >> 4) * 16);
+  const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB + ((lane >> 3) & 1) * 16);
+  const float sl2 = p.scale_log2;
+
+  for (int k = 0; k < my_tiles; ++k) {
+    issue(k + C::DEPTH - 1);
+    cp_async_wait<C::DEPTH - 1>();  // tile k has landed (for this lane's copies)
+    const int j = warp + k * kWarps;
     const int nv = min(C::TW, t_end - (t_begin + j * C::TW));
-    const uint8_t* kt = ring + s * C::STAGE_BYTES;
-    const uint8_t* vt = kt + C::TILE_BYTES;
-
-    // ---- scores s[g] = (scale*log2e*q_g) . k_r over this lane's part of D
-    float sc[GT];
-    {
-      float2 a[C::CHAINS][GT];
-#pragma unroll
-      for (int c = 0; c < C::CHAINS; ++c)
-#pragma unroll
-        for (int g = 0; g < GT; ++g) a[c][g] = make_float2(0.f, 0.f);
-      const uint8_t* krow = kt + r * C::ROWB + hf * (C::QH * 2);
-#pragma unroll
-      for (int c = 0; c < C::QH / 8; ++c) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(krow + c * 16);
-        const float2 k0 = unpack2<T>(kw.x), k1 = unpack2<T>(kw.y);
-        const float2 k2 = unpack2<T>(kw.z), k3 = unpack2<T>(kw.w);
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-          const float* qr = q_s + (g * C::LPT + hf) * C::QROW + c * 8;
-          const float4 qa = *reinterpret_cast<const float4*>(qr);
-          const float4 qb = *reinterpret_cast<const float4*>(qr + 4);
-          a[0][g] = ffma2(make_float2(qa.x, qa.y), k0, a[0][g]);
-          a[C::CHAINS - 1][g] = ffma2(make_float2(qa.z, qa.w), k1, a[C::CHAINS - 1][g]);
-          a[0][g] = ffma2(make_float2(qb.x, qb.y), k2, a[0][g]);
-          a[C::CHAINS - 1][g] = ffma2(make_float2(qb.z, qb.w), k3, a[C::CHAINS - 1][g]);
-        }
-      }
-      const bool live = r < nv;
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        float v = a[0][g].x + a[0][g].y;
-        if (C::CHAINS == 2) v += a[C::CHAINS - 1][g].x + a[C::CHAINS - 1][g].y;
-        if (C::LPT == 2) v += __shfl_xor_sync(0xffffffffu, v, 16);
-        sc[g] = live ? v : -INFINITY;  // select, so garbage or NaN in a dead row is dropped
+    const uint32_t kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
+    const uint32_t vt = kt + C::TILE_BYTES;
+    if (nv < C::TW) {
+      // rows past seq_len were never loaded: zero them in V so that p = 0 meets 0
+      uint8_t* vrow = my_ring + (k % C::DEPTH) * C::SLOT_BYTES + C::TILE_BYTES;
+      for (int i = lane; i < (C::TW - nv) * C::CPR; i += 32) {
+        const int r = nv + i / C::CPR, c = i % C::CPR;
+        *reinterpret_cast<uint4*>(vrow + r * C::ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    __syncwarp();  // every lane's copies (and the zero rows) are visible
 
-    // ---- online softmax (exp2 domain); p goes to shared memory for the PV phase
+    // ---- scores S^T[token][head] = K_tile . q^T (fp32 accumulate)
+    float s[NT][4];
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      float mt = sc[g];
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-      for (int o = C::TW / 2; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const float mn = fmaxf(m[g], mt);
-      const float mref = mn == -INFINITY ? 0.f : mn;
-      const float alpha = exp2f(m[g] - mref);
-      const float pv = exp2f(sc[g] - mref);
-      l[g] = l[g] * alpha + (hf == 0 ? pv : 0.f);
-      m[g] = mn;
-      const float2 a2 = make_float2(alpha, alpha);
+    for (int kk = 0; kk < C::KS; ++kk) {
+      uint32_t a[4];
+      ldmatrix_x4<false>(a, kt + k_lane + kk * 32);
 #pragma unroll
-      for (int i = 0; i < C::DPL / 2; ++i) acc[g][i] = fmul2(acc[g][i], a2);
-      if (hf == 0) pw[r * C::GP + g] = pv;
+      for (int nt = 0; nt < NT; ++nt) mma16816<T>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
     }
-    __syncwarp();
+    // rows gid and gid + 8 of the tile; -inf by select past seq_len
+    const bool live0 = gid < nv, live1 = gid + 8 < nv;
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float x0 = live0 ? s[nt][0] * sl2 : -INFINITY;
+      float x1 = live0 ? s[nt][1] * sl2 : -INFINITY;
+      float x2 = live1 ? s[nt][2] * sl2 : -INFINITY;
+      float x3 = live1 ? s[nt][3] * sl2 : -INFINITY;
+      // tile max per head over the 16 tokens (lanes sharing tig)
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+      }
+      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m[nt][0] - r0), al1 = exp2f(m[nt][1] - r1);
+      m[nt][0] = mn0;
+      m[nt][1] = mn1;
+      const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1);
+      const float p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
+      l[nt][0] = l[nt][0] * al0 + p0 + p2;
+      l[nt][1] = l[nt][1] * al1 + p1 + p3;
+#pragma unroll
+      for (int dd = 0; dd < C::KS; ++dd) {
+        o[nt][dd][0] *= al0;
+        o[nt][dd][1] *= al1;
+        o[nt][dd][2] *= al0;
+        o[nt][dd][3] *= al1;
+      }
+      // P^T[token][head] fragments -> P[head][token] as the B operand of PV
+      pb[nt][0] = movmatrix_trans(pack2<T>(p0, p1));
+      pb[nt][1] = movmatrix_trans(pack2<T>(p2, p3));
+    }
 
-    // ---- acc[g][:] += p[g][t] * v_t over live tokens only
-    const uint8_t* vcol = vt + lane * (C::DPL * 2);
-#pragma unroll 2
-    for (int t = 0; t < nv; ++t) {
-      float2 vv[C::DPL / 2];
-      if constexpr (C::DPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(vcol + t * C::ROWB);
-        vv[0] = unpack2<T>(w.x);
-        vv[1] = unpack2<T>(w.y);
-      } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(vcol + t * C::ROWB);
-        vv[0] = unpack2<T>(w.x);
-        vv[1] = unpack2<T>(w.y);
-        vv[2] = unpack2<T>(w.z);
-        vv[3] = unpack2<T>(w.w);
-      }
-      const float* pr = pw + t * C::GP;
+    // ---- O^T[d][head] += V_tile^T . P^T
 #pragma unroll
-      for (int g4 = 0; g4 < C::GP / 4; ++g4) {
-        const float4 p4 = *reinterpret_cast<const float4*>(pr + g4 * 4);
-        const float pg[4] = {p4.x, p4.y, p4.z, p4.w};
+    for (int dd = 0; dd < C::KS; ++dd) {
+      uint32_t a[4];
+      ldmatrix_x4<true>(a, vt + v_lane + dd * 32);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = g4 * 4 + k;
-          if (g < GT) {
-            const float2 pp = make_float2(pg[k], pg[k]);
-#pragma unroll
-            for (int i = 0; i < C::DPL / 2; ++i) acc[g][i] = ffma2(pp, vv[i], acc[g][i]);
-          }
-        }
-      }
+      for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][dd], a, pb[nt][0], pb[nt][1]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    __syncwarp();  // every lane is done with this slot before it is refilled
   }
+  cp_async_wait<0>();
 
-  // ---- denominators: sum the per-lane partial sums
+  // ---- denominators: sum over the 8 lanes that share tig (different tokens)
 #pragma unroll
-  for (int g = 0; g < GT; ++g)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) l[nt][h] += __shfl_xor_sync(0xffffffffu, l[nt][h], o2);
 
-  // ---- merge the consumer warps (the ring is free: every tile was consumed)
-  named_bar_sync(kMergeBar, kConsumerThreads);
+  // ---- merge the warps (the ring is free: every copy has landed and been consumed)
+  __syncthreads();
   float* mw = reinterpret_cast<float*>(ring);  // [NW][GT]
-  float* lw = mw + kConsumerWarps * GT;        // [NW][GT]
-  float* aw = lw + kConsumerWarps * GT;        // [NW][GT][D]
-  if (lane == 0)
+  float* lw = mw + kWarps * GT;                // [NW][GT]
+  float* aw = lw + kWarps * GT;                // [NW][GT][D]
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      mw[warp * GT + g] = m[g];
-      lw[warp * GT + g] = l[g];
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g0 = nt * 8 + 2 * tig;
+    if (gid == 0) {
+      mw[warp * GT + g0] = m[nt][0];
+      mw[warp * GT + g0 + 1] = m[nt][1];
+      lw[warp * GT + g0] = l[nt][0];
+      lw[warp * GT + g0 + 1] = l[nt][1];
     }
 #pragma unroll
-  for (int g = 0; g < GT; ++g)
-#pragma unroll
-    for (int i = 0; i < C::DPL / 2; ++i)
-      *reinterpret_cast<float2*>(aw + (warp * GT + g) * D + lane * C::DPL + 2 * i) = acc[g][i];
-  named_bar_sync(kMergeBar, kConsumerThreads);
+    for (int dd = 0; dd < C::KS; ++dd) {
+      const int d0 = dd * 16 + gid;
+      aw[(warp * GT + g0) * D + d0] = o[nt][dd][0];
+      aw[(warp * GT + g0 + 1) * D + d0] = o[nt][dd][1];
+      aw[(warp * GT + g0) * D + d0 + 8] = o[nt][dd][2];
+      aw[(warp * GT + g0 + 1) * D + d0 + 8] = o[nt][dd][3];
+    }
+  }
+  __syncthreads();
 
   const bool single = n_splits == 1;
   const size_t pidx = ((size_t)b * p.Hkv + kvh) * p.S + split;
-  for (int i = ctid; i < G * D; i += kConsumerThreads) {
+  for (int i = threadIdx.x; i < G * D; i += kThreads) {
     const int g = i / D, d = i - (i / D) * D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * GT + g]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GT + g]);
     float num = 0.f, den = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       const float e = exp2f(mw[w * GT + g] - M);  // idle warps: m = -inf, weight 0
       num += e * aw[(w * GT + g) * D + d];
       den += e * lw[w * GT + g];
@@ -357,54 +360,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       }
     }
   }
-  if (single) return;
+}
 
-  // ---- split merge by whichever CTA of this (sequence, KV head) finishes last
-  __threadfence();
-  named_bar_sync(kMergeBar, kConsumerThreads);
-  if (ctid == 0) {
-    const uint32_t done = atomicAdd(p.counters + (size_t)b * p.Hkv + kvh, 1u);
-    flag_s[0] = done == (uint32_t)(n_splits - 1);
-  }
-  named_bar_sync(kMergeBar, kConsumerThreads);
-  if (!flag_s[0]) return;
-  __threadfence();
-
+// Combine the split partials of one (sequence, query head, 64-wide slice of D):
+//   M = max_s m_s,  w_s = 2^(m_s - M),  out = sum_s w_s acc_s / sum_s w_s l_s
+// (the flash-decoding reduction). Every split holds at least one live token, so
+// m_s is finite and the weights are well defined. 256 threads: 64 output
+// elements x 4 split lanes.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  pdl_wait();  // the partials of the decode grid are complete and visible
+  pdl_launch_dependents();
+  __shared__ float ms[kMaxSplits], ws[kMaxSplits];
+  __shared__ float red[8], part[4][64];
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int G = p.G, kvh = h / G, g = h - kvh * G;
+  int L = __ldg(p.seq_lens + b);
+  const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int n = (L + p.P - 1) / p.P;
+  if (n <= 1) return;  // written by the decode grid
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
-  float* wts = reinterpret_cast<float*>(ring);  // [n_splits][GT]
-  float* Ms = wts + kMaxSplits * GT;            // [GT]
-  float* dens = Ms + GT;                        // [GT]
-  for (int g = ctid; g < G; g += kConsumerThreads) {
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < n_splits; ++s2) M = fmaxf(M, __ldcg(p.ws_m + (base + s2) * G + g));
-    Ms[g] = M;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  float mx = -INFINITY;
+  for (int s2 = tid; s2 < n; s2 += 256) {
+    const float v = __ldcg(p.ws_m + (base + s2) * G + g);
+    ms[s2] = v;
+    ws[s2] = __ldcg(p.ws_l + (base + s2) * G + g);
+    mx = fmaxf(mx, v);
   }
-  named_bar_sync(kMergeBar, kConsumerThreads);
-  for (int i = ctid; i < n_splits * G; i += kConsumerThreads) {
-    const int s2 = i / G, g = i - (i / G) * G;
-    wts[s2 * GT + g] = exp2f(__ldcg(p.ws_m + (base + s2) * G + g) - Ms[g]);
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float den = 0.f;
+  for (int s2 = tid; s2 < n; s2 += 256) {
+    const float w = exp2f(ms[s2] - M);
+    den += w * ws[s2];
+    ms[s2] = w;  // ms now holds the weights
   }
-  named_bar_sync(kMergeBar, kConsumerThreads);
-  for (int g = ctid; g < G; g += kConsumerThreads) {
-    float den = 0.f;
-    for (int s2 = 0; s2 < n_splits; ++s2) den += wts[s2 * GT + g] * __ldcg(p.ws_l + (base + s2) * G + g);
-    dens[g] = den;
+  for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) red[warp] = den;
+  __syncthreads();
+  den = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) den += red[w];
+
+  const int dl = tid & 63, sl = tid >> 6;
+  const int d = blockIdx.x * 64 + dl;
+  const float* acc = p.ws_acc + (base * G + g) * D + d;
+  float num = 0.f;
+#pragma unroll 8
+  for (int s2 = sl; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * G * D);
+  part[sl][dl] = num;
+  __syncthreads();
+  if (sl == 0) {
+    num = part[0][dl] + part[1][dl] + part[2][dl] + part[3][dl];
+    reinterpret_cast<T*>(p.out)[((size_t)b * p.Hq + h) * D + d] = from_f32<T>(num / den);
   }
-  named_bar_sync(kMergeBar, kConsumerThreads);
-  for (int i = ctid; i < G * D; i += kConsumerThreads) {
-    const int g = i / D, d = i - (i / D) * D;
-    float num = 0.f;
-    for (int s2 = 0; s2 < n_splits; ++s2)
-      num += wts[s2 * GT + g] * __ldcg(p.ws_acc + ((base + s2) * G + g) * D + d);
-    out[(head0 + g) * D + d] = from_f32<T>(num / dens[g]);
-  }
-  if (ctid == 0) p.counters[(size_t)b * p.Hkv + kvh] = 0u;  // ready for the next call
 }
 
 // ------------------------------------------------------------------ launch
-template <typename T, int D, int GT>
-cudaError_t launch_decode_gt(const DecodeParams& p, cudaStream_t st) {
-  using C = Cfg<D, GT>;
+// Launch with programmatic stream serialization: the grid may start while the
+// previous kernel in the stream finishes; its pdl_wait() orders the reads.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const DecodeParams& p) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <typename T, int D, int NT>
+cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
+  using C = Cfg<D, NT>;
   // The dynamic shared memory opt-in is per device; remember which devices have it.
   static unsigned long long done_mask = 0ull;
   int dev = 0;
@@ -412,29 +453,20 @@ cudaError_t launch_decode_gt(const DecodeParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_kernel<T, D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  const dim3 grid(p.S, p.Hkv, p.B);
-  decode_kernel<T, D, GT><<<grid, kThreads, C::SMEM, st>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(decode_kernel<T, D, NT>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
+  if (e != cudaSuccess) return e;
+  if (p.S > 1) e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq, p.B), dim3(256), 0, st, p);
+  return e;
 }
 
 template <typename T, int D>
 cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st) {
-  switch (p.G) {
-    case 1: return launch_decode_gt<T, D, 1>(p, st);
-    case 2: return launch_decode_gt<T, D, 2>(p, st);
-    case 3: return launch_decode_gt<T, D, 3>(p, st);
-    case 4: return launch_decode_gt<T, D, 4>(p, st);
-    case 5: return launch_decode_gt<T, D, 5>(p, st);
-    case 6: return launch_decode_gt<T, D, 6>(p, st);
-    case 7: return launch_decode_gt<T, D, 7>(p, st);
-    case 8: return launch_decode_gt<T, D, 8>(p, st);
-    default: return launch_decode_gt<T, D, 16>(p, st);  // 9..16: padded heads are zero
-  }
+  return p.G <= 8 ? launch_decode_nt<T, D, 1>(p, st) : launch_decode_nt<T, D, 2>(p, st);
 }
 
 }  // namespace pa

@@ -9,11 +9,12 @@
 namespace pa {
 
 // Tokens staged per CTA are bounded by the block-table slice it keeps in shared
-// memory; split counts are bounded by the merge scratch of the last CTA.
+// memory; split counts are bounded by the merge kernel's shared weights.
 constexpr int kBtMax = 1024;
 constexpr int kMaxSplits = 1024;
-constexpr int kPartitionMin = 128;  // tokens: below this a split's fixed cost dominates
-constexpr int kTokenQuantum = 32;   // partition sizes are multiples of the warp tile
+constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost dominates
+constexpr int kTokenQuantum = 16;   // partition sizes are multiples of the warp tile
+constexpr int kSplitOverhead = 64;  // a CTA's fixed cost, in tokens, for the split planner
 
 struct DecodeParams {
   const void* q;
@@ -25,7 +26,6 @@ struct DecodeParams {
   float* ws_m;        // [B*Hkv*S][G]   running max of each split (log2 domain)
   float* ws_l;        // [B*Hkv*S][G]   softmax denominator of each split
   float* ws_acc;      // [B*Hkv*S][G][D] unnormalised output of each split
-  uint32_t* counters; // [B*Hkv]        splits finished, reset by the merging CTA
   uint32_t* err;      // device error word
   int B, Hq, Hkv, G;
   int block_size, num_blocks, max_blocks, max_seq_len;

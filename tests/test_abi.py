@@ -69,6 +69,7 @@ def _call(lib, a, ws=256, nbytes=1 << 20):
     (dict(q=0), pa.PA_ERR_INVALID_ARG),
     (dict(out=0), pa.PA_ERR_INVALID_ARG),
     (dict(k_cache=40), pa.PA_ERR_INVALID_ARG),              # not 16-byte aligned
+    (dict(num_blocks=1 << 24, block_size=784, Hkv=8, Hq=8), pa.PA_ERR_UNSUPPORTED),  # rows > 2^32
 ])
 def test_host_validation(lib, kw, code):
     assert _call(lib, _args(**kw)) == code
@@ -107,21 +108,21 @@ SM = 152
 ])
 def test_plan_properties(lib, B, Hkv, bs, L):
     S, P = pa.plan(B, Hkv * 2, Hkv, 128, bs, L, sm_count=SM)
-    assert P % 32 == 0 and P > 0
+    assert P % 16 == 0 and P > 0
     assert S * P >= L, "the splits cover the longest context"
     assert (S - 1) * P < L, "no split of the longest context is empty"
     assert S <= 1024
     assert (P - 1) // bs + 2 <= 1024, "a split's block-table slice fits the CTA buffer"
-    # every SM gets a split unless that would make splits shorter than 128 tokens
-    assert B * Hkv * S >= SM or P <= 160
+    # the plan never leaves more than one wave partly empty when splits can be short
+    waves = -(-B * Hkv * S // SM)
+    assert waves <= 4 or S == 1 or P >= 16352
 
 
 def test_plan_fills_sms_at_batch_one():
     S, P = pa.plan(1, 24, 4, 256, 784, 32768, sm_count=SM)
-    assert 4 * S >= SM
+    assert 4 * S == SM            # one full wave: 37 splits of 896 tokens
     S, P = pa.plan(1, 24, 4, 256, 784, 4096, sm_count=SM)
-    assert 4 * S >= 4096 // 128  # bounded by the minimum split length
-    assert P == 128
+    assert 4 * S <= SM and P == 112   # one wave of 112-token splits
 
 
 def test_forced_splits():
@@ -129,7 +130,7 @@ def test_forced_splits():
         S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=want, sm_count=SM)
         assert S == want and S * P >= 1025
     S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=10000, sm_count=SM)
-    assert P == 32 and S == 33
+    assert P == 16 and S == 65
 
 
 def test_large_batch_needs_no_split():

@@ -190,6 +190,20 @@ def test_split_sweep_head256(cuda_lib):
         assert_parity(to_np(run(cuda_lib, case, splits=S)), ref, what=f"d256 splits={S}")
 
 
+def test_workspace_reused_across_shapes(cuda_lib):
+    # one workspace, calls of different (B, Hkv, splits) in a row: each call must
+    # find its counters at zero whatever the previous call stored in the partials
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    for B, hq, hkv, L in [(8, 32, 8, 1024), (8, 32, 16, 1024), (2, 64, 64, 2500),
+                          (1, 24, 4, 3000), (8, 32, 16, 4096)]:
+        D = 256 if hkv == 4 else 128
+        bs = 784 if hkv == 4 else 16
+        case = pi.make_case(B, hq, hkv, D, bs, [L] * B, seed=B + hkv)
+        y = run(cuda_lib, case, workspace=ws)
+        assert_parity(to_np(y), oracle_case(case), what=f"reuse {B}x{hq}/{hkv} L={L}")
+        assert cuda_lib.read_device_errors(ws) == 0
+
+
 # ------------------------------------------------------------------ invariances
 def test_block_permutation_invariance(cuda_lib):
     case = pi.make_case(3, 32, 8, 128, 16, [3001, 17, 4096], seed=11, poison="kv_nan")
