@@ -157,6 +157,38 @@ pa_status pa_read_device_errors(void* workspace, pa_stream_t stream, uint32_t* f
 /* Make `device` current for this library's calls on the calling thread. */
 pa_status pa_set_device(int device);
 
+/*
+ * pa_decode without a workspace, for callers that cannot allocate device memory
+ * or pass scratch to the library: for example a plugin inside another runtime
+ * that owns all device allocations, code that must not call cudaMalloc because
+ * it may synchronise the device, or a binding with no device allocator. The pages
+ * describe no such call; it exists only for those callers.
+ *
+ * Arguments, layouts, validation and results are those of pa_decode. The split
+ * partials live in one array of PA_NOALLOC_SCRATCH_BYTES that is part of this
+ * library's device image: every GPU that loads it keeps that memory until the
+ * process exits, and the call itself allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *  - Limit: a call whose partials need more than PA_NOALLOC_SCRATCH_BYTES (as
+ *    pa_decode_workspace_bytes reports) returns PA_ERR_WORKSPACE and launches
+ *    nothing; use pa_decode with your own workspace for it.
+ *  - The first call on a device looks up the array's device address and zeroes
+ *    its header (a synchronous cudaMemset); make that first call before any
+ *    stream capture on that device.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents. Nothing in it needs to start at zero except the error word,
+ *    cleared at that first call. Calls that may overlap on the GPU (different
+ *    streams, concurrent threads) race on it: serialise them.
+ *  - Device-side range errors (PA_DEVERR_*) are recorded in the array's header
+ *    and are not readable through this API.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                            int B, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                            int max_blocks_per_seq, int max_seq_len, float scale,
+                            pa_dtype dtype, pa_stream_t stream);
+
 /* Static text for a status code. */
 const char* pa_status_string(pa_status status);
 

@@ -38,6 +38,8 @@ SIGNATURES = {
     "pa_decode": (_c.c_int, [_c.c_void_p] * 6 + [_c.c_int] * 8 +
                   [_c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "pa_decode_ex": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "pa_decode_noalloc": (_c.c_int, [_c.c_void_p] * 6 + [_c.c_int] * 8 +
+                          [_c.c_float, _c.c_int, _c.c_void_p]),
     "pa_decode_plan": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_void_p, _c.c_void_p]),
     "pa_workspace_init": (_c.c_int, [_c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "pa_read_device_errors": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p]),
@@ -210,6 +212,26 @@ def decode_plain(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None,
                        args.scale, args.dtype, ws.data_ptr(), ws.numel(), sh)
     if rc != PA_OK:
         raise PAError(rc, "pa_decode")
+    return out
+
+
+def decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None,
+                   max_seq_len: Optional[int] = None, stream=None):
+    """The same operation through pa_decode_noalloc: no workspace, no allocation by
+    the library (the split partials live in a fixed device array of the library,
+    shared by all such calls on a device; see include/pa.h for the limit)."""
+    lib = load()
+    if out is None:
+        out = torch.empty_like(q)
+    args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, 0)
+    _ensure_device(lib, q.device.index)
+    sh = _stream_handle(q.device, stream)
+    rc = lib.pa_decode_noalloc(args.q, args.k_cache, args.v_cache, args.block_tables,
+                               args.seq_lens, args.out, args.B, args.Hq, args.Hkv, args.D,
+                               args.block_size, args.num_blocks, args.max_blocks_per_seq,
+                               args.max_seq_len, args.scale, args.dtype, sh)
+    if rc != PA_OK:
+        raise PAError(rc, "pa_decode_noalloc")
     return out
 
 
