@@ -23,8 +23,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // multiple of the 16-token warp tile). The unit of parallel work is a (sequence,
 // KV head, split) CTA, one resident per SM. The cost of a plan is the number of
 // CTA waves times the tokens a CTA streams plus its fixed cost; candidates are
-// one split and the largest split counts that fill exactly 1..4 waves. P is also
-// bounded so that a split's block-table slice fits the CTA's staging buffer.
+// one split and the largest split counts that fill exactly 1..4 waves.
 struct Plan {
   int S;
   int P;
@@ -44,18 +43,16 @@ bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, Plan*
   return true;
 }
 
-bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t max_len,
-               int requested, Plan* out) {
+bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_size,
+               int64_t max_len, int requested, Plan* out) {
   if (max_len <= 0) {
     *out = {1, pa::kTokenQuantum};
     return true;
   }
   const int64_t units = B * Hkv;
   const int64_t sm = sm_count > 0 ? sm_count : 1;
-  const int64_t p_max =
-      std::max<int64_t>(pa::kTokenQuantum,
-                        ((int64_t)(pa::kBtMax - 2) * block_size) / pa::kTokenQuantum *
-                            pa::kTokenQuantum);
+  (void)block_size;
+  const int64_t p_max = round_up(max_len, pa::kTokenQuantum);
   if (requested > 0) return plan_for(requested, max_len, p_max, false, out);
   bool found = false;
   int64_t best_cost = 0;
@@ -66,7 +63,8 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t block_size, int64_t
     Plan pl{};
     if (!plan_for(c, max_len, p_max, true, &pl)) continue;
     const int64_t waves = ceil_div(units * pl.S, sm);
-    const int64_t cost = waves * (pl.P + pa::kSplitOverhead);
+    const int64_t overhead_tokens = pa::kSplitOverheadBytes / (4 * D);  // K + V bytes per token
+    const int64_t cost = waves * (pl.P + overhead_tokens);
     if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
       *out = pl;
       best_cost = cost;
@@ -176,7 +174,7 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
   if (sm_count <= 0) sm_count = current_sm_count();
   if (sm_count <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm_count, a->B, a->Hkv, a->block_size, max_len, a->splits, &plan))
+  if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, max_len, a->splits, &plan))
     return PA_ERR_UNSUPPORTED;
   *splits = plan.S;
   *partition_tokens = plan.P;
@@ -244,7 +242,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const int sm = current_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm, a->B, a->Hkv, a->block_size, max_len, a->splits, &plan))
+  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, max_len, a->splits, &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const WsLayout w = ws_layout(a->B, a->Hkv, G, a->D, plan.S);

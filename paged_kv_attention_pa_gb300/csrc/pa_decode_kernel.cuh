@@ -36,7 +36,7 @@
 #include "pa_params.h"
 
 #ifndef PA_WARPS_D128
-#define PA_WARPS_D128 4
+#define PA_WARPS_D128 8
 #endif
 #ifndef PA_WARPS_D256
 #define PA_WARPS_D256 4
@@ -59,8 +59,7 @@ struct Cfg {
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static constexpr int KS = D / 16;             // k-steps of the score MMA = d-blocks of PV
   static constexpr int COPIES = TW * CPR / 32;  // 16-byte copies per lane per operand per tile
-  static constexpr int BT_BYTES = kBtMax * 4;
-  static constexpr int FIXED = BT_BYTES + 256;
+  static constexpr int FIXED = 256;
   static constexpr int DEPTH_FIT = (kSmemBudget - FIXED) / (NW * SLOT_BYTES);
   static constexpr int DEPTH = DEPTH_FIT > 12 ? 12 : DEPTH_FIT;  // slots per warp
   static constexpr int RING = NW * DEPTH * SLOT_BYTES;
@@ -91,7 +90,6 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   constexpr int kThreads = C::THREADS;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  int* bt_s = reinterpret_cast<int*>(smem + C::RING);
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -109,46 +107,24 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   pdl_wait();
   pdl_launch_dependents();
 
-  // ---- context length, validated against the bounds the launch was planned for
-  int L = __ldg(p.seq_lens + b);
-  {
-    const long long cap_ll = (long long)p.max_blocks * p.block_size;
-    const int cap = (int)min((long long)p.max_seq_len, cap_ll);
-    if (L < 0 || L > cap) {
-      if (split == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
-      L = L < 0 ? 0 : cap;
-    }
-  }
-  if (L == 0) {  // empty context: a zero row, written once
-    if (split == 0)
-      for (int i = threadIdx.x; i < G * D; i += kThreads) out[head0 * D + i] = from_f32<T>(0.f);
-    return;
-  }
+  // ---- prologue: everything the first copies depend on is requested at once (one
+  // round trip): the context length, the query fragments and, speculatively, the
+  // block-table entries of this warp's first tiles. Entries are read only inside
+  // the table row; those past the sequence are ignored, never dereferenced.
+  const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks;
   const int t_begin = split * p.P;
-  if (t_begin >= L) return;  // this split lies past the sequence: nothing to do
-  const int t_end = min(L, t_begin + p.P);
-  const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
-  const int n_splits = (L + p.P - 1) / p.P;
-
-  // ---- this split's block-table slice, validated
-  const int blk0 = t_begin / p.block_size;
-  int nb = (t_end - 1) / p.block_size - blk0 + 1;
-  if (nb > kBtMax) {  // the planner never allows this; stay in bounds regardless
-    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
-    nb = kBtMax;
-  }
-  {
-    const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks;
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-      int phys = __ldg(bt_row + blk0 + i);
-      if (phys < 0 || phys >= p.num_blocks) {
-        atomicOr(p.err, PA_DEVERR_BLOCK_INDEX);
-        phys = 0;
-      }
-      bt_s[i] = phys;
-    }
-  }
-  // ---- query fragments (B operand of the score MMA), unscaled, zero for padded heads
+  const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
+  // block-table entry of token t0(k) + lane, for this warp's k-th tile
+  auto table_entry = [&](int k) -> int {
+    const long long t = (long long)t_begin + (long long)(warp + k * kWarps) * C::TW + lane;
+    if (lane >= C::TW || t >= cap) return 0;
+    return __ldg(bt_row + (int)t / p.block_size);
+  };
+  int pe[C::DEPTH];  // entries of tiles 0 .. DEPTH-1
+#pragma unroll
+  for (int k = 0; k < C::DEPTH; ++k) pe[k] = table_entry(k);
+  int L = __ldg(p.seq_lens + b);
+  // query fragments (B operand of the score MMA), unscaled, zero for padded heads
   uint32_t qf[NT][C::KS][2];
   {
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
@@ -164,7 +140,21 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
       }
     }
   }
-  __syncthreads();
+
+  // ---- context length, validated against the bounds the launch was planned for
+  if (L < 0 || L > cap) {
+    if (split == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
+    L = L < 0 ? 0 : cap;
+  }
+  if (L == 0) {  // empty context: a zero row, written once
+    if (split == 0)
+      for (int i = threadIdx.x; i < G * D; i += kThreads) out[head0 * D + i] = from_f32<T>(0.f);
+    return;
+  }
+  if (t_begin >= L) return;  // this split lies past the sequence: nothing to do
+  const int t_end = min(L, t_begin + p.P);
+  const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
+  const int n_splits = (L + p.P - 1) / p.P;
 
   // ---- per-warp copy pipeline
   const uint64_t pol = l2_evict_first_policy();
@@ -175,8 +165,9 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   const uint32_t my_ring_s = smem_addr(my_ring);
   const int my_tiles = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
 
-  // Issue the copies of this warp's k-th tile (a commit group even when empty).
-  auto issue = [&](int k) {
+  // Issue the copies of this warp's k-th tile (a commit group even when empty);
+  // phys is this lane's block-table entry for the tile, validated here.
+  auto issue = [&](int k, int phys) {
     if (k < my_tiles) {
       const int j = warp + k * kWarps;
       const int t0 = t_begin + j * C::TW;
@@ -185,9 +176,11 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
       uint32_t ridx = 0;
       if (lane < nv) {
         const int t = t0 + lane;
-        const int lb = t / p.block_size;
-        const int off = t - lb * p.block_size;
-        const int phys = bt_s[min(lb - blk0, nb - 1)];
+        const int off = t - (t / p.block_size) * p.block_size;
+        if ((unsigned)phys >= (unsigned)p.num_blocks) {
+          atomicOr(p.err, PA_DEVERR_BLOCK_INDEX);
+          phys = 0;
+        }
         ridx = ((uint32_t)phys * (uint32_t)p.block_size + (uint32_t)off) * (uint32_t)p.Hkv +
                (uint32_t)kvh;
       }
@@ -209,7 +202,8 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   };
 
 #pragma unroll
-  for (int k = 0; k < C::DEPTH - 1; ++k) issue(k);
+  for (int k = 0; k < C::DEPTH - 1; ++k) issue(k, pe[k]);
+  int next_entry = pe[C::DEPTH - 1];  // for the tile issued in the first loop iteration
 
   // running state: this thread's heads are nt*8 + 2*tig + {0, 1}
   float m[NT][2], l[NT][2];
@@ -227,7 +221,9 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   const float sl2 = p.scale_log2;
 
   for (int k = 0; k < my_tiles; ++k) {
-    issue(k + C::DEPTH - 1);
+    const int entry = next_entry;
+    next_entry = table_entry(k + C::DEPTH);  // one iteration ahead of its use
+    issue(k + C::DEPTH - 1, entry);
     cp_async_wait<C::DEPTH - 1>();  // tile k has landed (for this lane's copies)
     const int j = warp + k * kWarps;
     const int nv = min(C::TW, t_end - (t_begin + j * C::TW));
@@ -382,6 +378,19 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   if (n <= 1) return;  // written by the decode grid
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int dl = tid & 63, sl = tid >> 6;
+  const int d = blockIdx.x * 64 + dl;
+  const float* acc = p.ws_acc + (base * G + g) * D + d;
+
+  // The accumulators do not depend on the weights: request the first 16 splits of
+  // this thread's lane together with the maxima and sums (one round trip).
+  constexpr int kPre = 16;
+  float av[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int s2 = sl + 4 * i;
+    av[i] = s2 < n ? __ldcg(acc + (size_t)s2 * G * D) : 0.f;
+  }
 
   float mx = -INFINITY;
   for (int s2 = tid; s2 < n; s2 += 256) {
@@ -410,12 +419,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
 #pragma unroll
   for (int w = 0; w < 8; ++w) den += red[w];
 
-  const int dl = tid & 63, sl = tid >> 6;
-  const int d = blockIdx.x * 64 + dl;
-  const float* acc = p.ws_acc + (base * G + g) * D + d;
   float num = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int s2 = sl + 4 * i;
+    if (s2 < n) num += ms[s2] * av[i];
+  }
 #pragma unroll 8
-  for (int s2 = sl; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * G * D);
+  for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * G * D);
   part[sl][dl] = num;
   __syncthreads();
   if (sl == 0) {

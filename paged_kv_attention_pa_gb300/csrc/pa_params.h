@@ -8,13 +8,16 @@
 
 namespace pa {
 
-// Tokens staged per CTA are bounded by the block-table slice it keeps in shared
-// memory; split counts are bounded by the merge kernel's shared weights.
-constexpr int kBtMax = 1024;
+// Split counts are bounded by the merge kernel's shared weights.
 constexpr int kMaxSplits = 1024;
 constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost dominates
 constexpr int kTokenQuantum = 16;   // partition sizes are multiples of the warp tile
-constexpr int kSplitOverhead = 64;  // a CTA's fixed cost, in tokens, for the split planner
+#ifndef PA_SPLIT_OVERHEAD_BYTES
+#define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
+#endif
+// A CTA's fixed cost (launch, first round trip, epilogue) expressed as the KV bytes
+// it could have streamed meanwhile; the split planner charges it once per CTA.
+constexpr int kSplitOverheadBytes = PA_SPLIT_OVERHEAD_BYTES;
 
 struct DecodeParams {
   const void* q;

@@ -112,10 +112,9 @@ def test_plan_properties(lib, B, Hkv, bs, L):
     assert S * P >= L, "the splits cover the longest context"
     assert (S - 1) * P < L, "no split of the longest context is empty"
     assert S <= 1024
-    assert (P - 1) // bs + 2 <= 1024, "a split's block-table slice fits the CTA buffer"
     # the plan never leaves more than one wave partly empty when splits can be short
     waves = -(-B * Hkv * S // SM)
-    assert waves <= 4 or S == 1 or P >= 16352
+    assert waves <= 4 or S == 1
 
 
 def test_plan_fills_sms_at_batch_one():
