@@ -277,6 +277,19 @@ def oracle_sample(budget_s, shapes=GRID_SHAPES, lens=GRID_LENS, D=128, device="c
     return done_bytes, spent, "float64 oracle, batch-1 grid cells " + ",".join(cells)
 
 
+def aggregate_over_ranks(kv_bytes_per_rank, ms_step, e2e_ms, world, device):
+    """Whole-job values of a replicas run: every rank processed kv_bytes_per_rank per
+    step; the job's step time is the slowest rank's. Returns (value GB/s, e2e GB/s,
+    max step ms, max e2e ms)."""
+    t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max, e2e_max = float(t[0]), float(t[1])
+    value = world * kv_bytes_per_rank / (ms_max * 1e-3) / 1e9
+    e2e_value = world * kv_bytes_per_rank / (e2e_max * 1e-3) / 1e9
+    return value, e2e_value, ms_max, e2e_max
+
+
 # ---------------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The float64 CPU oracle as the reference arm (rank 0 only)."""
@@ -446,12 +459,7 @@ def run_ours(args, rank, world, local_rank):
     kv = sum(c.kv_bytes() for c in cells)
     alg = sum(c.alg_bytes() for c in cells)
     ms_step = total_ms / args.steps
-    t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_step_max, e2e_max = float(t[0]), float(t[1])
-    value = world * kv / (ms_step_max * 1e-3) / 1e9
-    e2e_value = world * kv / (e2e_max * 1e-3) / 1e9
+    value, e2e_value, ms_step_max, e2e_max = aggregate_over_ranks(kv, ms_step, e2e_ms, world, dev)
     if rank != 0:
         return
 
