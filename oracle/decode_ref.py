@@ -53,12 +53,16 @@ def decode_ref_one(q_g: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) 
 
 
 def decode_ref(q: np.ndarray, K_list: Sequence[np.ndarray], V_list: Sequence[np.ndarray],
-               scale: float) -> np.ndarray:
+               scale: float, window: int = 0) -> np.ndarray:
     """Decode for a whole batch.
 
     q: [B, Hq, D] float64. K_list[b], V_list[b]: [L_b, Hkv, D] float64, the
     contiguous (pre-paging) keys and values of sequence b. scale: the fp32 scale
-    widened to float64. Returns out [B, Hq, D] float64.
+    widened to float64. window > 0 restricts every query to the last `window`
+    tokens of its context, t in [max(0, L_b - window), L_b): the sliding-window
+    layers of "vLLM's custom ROCm paged-attention kernel wins all sixty cells" (§4:
+    a sliding layer scans 1024 tokens while a full layer scans the whole context).
+    window <= 0 is the full context. Returns out [B, Hq, D] float64.
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -66,6 +70,9 @@ def decode_ref(q: np.ndarray, K_list: Sequence[np.ndarray], V_list: Sequence[np.
     for b in range(B):
         K = np.asarray(K_list[b], dtype=np.float64)
         V = np.asarray(V_list[b], dtype=np.float64)
+        if window > 0:
+            lo = max(0, K.shape[0] - window)
+            K, V = K[lo:], V[lo:]
         if K.shape[0] == 0:
             continue
         Hkv = K.shape[1]

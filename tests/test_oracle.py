@@ -281,3 +281,38 @@ def test_rel_linf_error():
     y[1, 0] = np.nan
     assert rel_linf_error(y, r) == float("inf")
     assert rel_linf_error(np.zeros(3), np.zeros(3)) == 0.0
+
+
+# ----------------------------------------------------------------- sliding window
+def test_window_at_least_context_is_full_decode():
+    q, K, V, scale = _rand_problem(40, lens=(9, 5))
+    full = decode_ref(q, K, V, scale)
+    assert np.array_equal(decode_ref(q, K, V, scale, window=9), full)
+    assert np.array_equal(decode_ref(q, K, V, scale, window=100), full)
+    assert np.array_equal(decode_ref(q, K, V, scale, window=0), full)
+
+
+def test_window_one_returns_last_value_row():
+    q, K, V, scale = _rand_problem(41, lens=(9, 5))
+    y = decode_ref(q, K, V, scale, window=1)
+    for b, L in enumerate((9, 5)):
+        for h in range(4):
+            assert np.array_equal(y[b, h], V[b][L - 1, h // 2])
+
+
+def test_window_brute_force():
+    # the window is the last W tokens: brute force over exactly those tokens
+    q, K, V, scale = _rand_problem(42, lens=(8, 3))
+    W = 3
+    y = decode_ref(q, K, V, scale, window=W)
+    r = _brute_force_decimal(q, [k[-W:] for k in K], [v[-W:] for v in V], scale)
+    assert np.abs(y - r).max() <= 1e-14 * max(1.0, np.abs(r).max())
+
+
+def test_window_pins_catch_off_by_one():
+    # a plausible mistake (window starting one token late) fails the brute force pin
+    q, K, V, scale = _rand_problem(43, lens=(8, 6))
+    W = 4
+    wrong = decode_ref(q, [k[1:] for k in K], [v[1:] for v in V], scale, window=W - 1)
+    r = _brute_force_decimal(q, [k[-W:] for k in K], [v[-W:] for v in V], scale)
+    assert np.abs(wrong - r).max() > 1e-6
