@@ -19,7 +19,8 @@ rotating over enough independent copies of the cell (>= 512 MiB of KV in total,
 four times the L2) that every call reads HBM, as an engine replays its layers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload grid|hybrid|mixed|first|cell] [--cell Hq,Hkv,B,L,D,bs]
+                    [--workload grid|hybrid|mixed|first|cell|window]
+                    [--cell Hq,Hkv,B,L,D,bs]
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (there is no other implementation to run). With torchrun (N > 1) every
@@ -57,12 +58,16 @@ ROTATE_BYTES = 512 << 20  # KV per rotation of the steady-state curve (4x the 12
 class Inst:
     """One set of device inputs for a decode call."""
 
-    def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, exact):
+    def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, exact,
+                 window=0):
         gen = torch.Generator(device=device)
         gen.manual_seed(seed)
         dt = torch.bfloat16
         nblk = [-(-L // bs) for L in lens]
-        nb = max(1, int(math.ceil(sum(nblk) * pool_factor)))
+        # timing copies of a windowed call back only the blocks the window can touch;
+        # earlier logical blocks share them (they are never read)
+        back = [min(n, -(-window // bs) + 1) if (window > 0 and not exact) else n for n in nblk]
+        nb = max(1, int(math.ceil(sum(back) * pool_factor)))
         self.num_blocks = nb
         self.q = torch.randn((B, Hq, D), generator=gen, device=device).to(dt)
         if exact:
@@ -78,9 +83,13 @@ class Inst:
         bt = torch.full((B, max(nblk)), -1, dtype=torch.int32, device=device)
         off = 0
         for b, L in enumerate(lens):
-            n = nblk[b]
-            bt[b, :n] = perm[off:off + n].to(torch.int32)
-            off += n
+            n, m = nblk[b], back[b]
+            own = perm[off:off + m].to(torch.int32)
+            # the last m logical blocks get their own physical blocks, in order
+            bt[b, n - m:n] = own
+            if n > m:
+                bt[b, :n - m] = own[torch.arange(n - m, device=device) % m]
+            off += m
             if exact:
                 t = torch.arange(L, device=device)
                 phys = bt[b, (t // bs)].long()
@@ -95,8 +104,9 @@ class Cell:
     """A decode configuration: inputs for the step, plus copies for the curve."""
 
     def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison=None, pool_factor=2.0,
-                 tag=""):
+                 tag="", window=0):
         self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
+        self.window = window
         self.lens = list(lens)
         self.tag = tag
         self.seed, self.device, self.poison, self.pool_factor = seed, device, poison, pool_factor
@@ -109,20 +119,24 @@ class Cell:
         for i in range(len(self.insts), n):
             self.insts.append(Inst(self.B, self.Hq, self.Hkv, self.D, self.bs, self.lens,
                                    self.seed + 7919 * i, self.device, self.poison,
-                                   self.pool_factor, False))
+                                   self.pool_factor, False, self.window))
+
+    def read_lens(self):
+        """Tokens each sequence's query attends to (the window bounds them)."""
+        return [min(L, self.window) if self.window > 0 else L for L in self.lens]
 
     def kv_bytes(self) -> int:
-        return sum(self.lens) * self.Hkv * self.D * 2 * 2
+        return sum(self.read_lens()) * self.Hkv * self.D * 2 * 2
 
     def alg_bytes(self) -> int:
         """Bytes the method must move: KV, the live block-table entries, q, out, seq_lens."""
-        table = sum(-(-L // self.bs) for L in self.lens) * 4
+        table = sum(-(-L // self.bs) + 1 for L in self.read_lens()) * 4
         return self.kv_bytes() + table + 2 * self.B * self.Hq * self.D * 2 + 4 * self.B
 
     def call(self, pa, stream=None, i=0):
         x = self.insts[i]
         pa.decode(x.q, x.k, x.v, x.bt, x.sl, self.scale, out=x.out, max_seq_len=self.max_len,
-                  workspace=self.ws, stream=stream)
+                  workspace=self.ws, stream=stream, window=self.window)
 
 
 def parse_cell(spec):
@@ -162,6 +176,18 @@ def build_workload(name, device, seed=0, cell_spec=None):
         desc = {"workload": "mixed_serving_batch", "batch": 64, "Hq": 32, "Hkv": 8,
                 "head_dim": 128, "block_size": 16, "seq_lens": "U[1024,32768] seed 0",
                 "pool": "shared, 1.1x used blocks, NaN in unwritten slots"}
+    elif name == "window":
+        # sliding-window layers: 32 query / 16 KV heads, head 128, block 16, W = 1024
+        i = 0
+        for B in GRID_BATCHES:
+            for L in GRID_LENS:
+                cells.append(Cell(B, 32, 16, 128, 16, [L] * B, seed + i, device,
+                                  tag=f"window 32/16 B={B} L={L}", window=1024))
+                i += 1
+        desc = {"workload": "sliding_window_layer", "Hq": 32, "Hkv": 16, "head_dim": 128,
+                "block_size": 16, "window": 1024, "seq_lens": GRID_LENS,
+                "batches": GRID_BATCHES, "cells": len(cells),
+                "bytes": "KV of the window only: min(L, 1024) tokens per sequence"}
     elif name == "first":
         cells.append(Cell(1, 8, 8, 128, 16, [512], seed, device, tag="first"))
         desc = {"workload": "first_config", "batch": 1, "Hq": 8, "Hkv": 8, "head_dim": 128,
@@ -369,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
     # one workspace per cell so the captured graph has fixed addresses
     for c in cells:
         x = c.insts[0]
-        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len)
+        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len, 0, c.window)
         nbytes = lib.pa_decode_ex_workspace_bytes(ctypes.byref(a))
         c.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -476,9 +502,12 @@ def run_ours(args, rank, world, local_rank):
             c.add_copies(max(1, min(256, -(-ROTATE_BYTES // max(1, c.kv_bytes())))))
             us = steady_state_us(pa, c, stream)
             gbs = c.kv_bytes() / (us * 1e-6) / 1e9
-            S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len)
-            curve.append({"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
-                          "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)})
+            S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window)
+            entry = {"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)}
+            if len(members) == 16:  # the hybrid's 16 full-attention layers: one decode step
+                entry["ms_per_step_16_layers"] = round(16 * us / 1000.0, 4)
+            curve.append(entry)
             del c.insts[1:]
             torch.cuda.empty_cache()
 
@@ -496,7 +525,8 @@ def run_ours(args, rank, world, local_rank):
                   f"({kv / 2**30:.2f} GiB of distinct KV per step)",
             "timed": "CUDA graph of the whole step, replayed K times, CUDA events",
             "kv_bytes_per_step": kv}),
-        "gpu_launches": sum(2 if pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len)[0] > 1 else 1
+        "gpu_launches": sum(2 if pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len,
+                                         window=c.window)[0] > 1 else 1
                             for c in cells) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
@@ -527,7 +557,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="grid",
-                    choices=["grid", "hybrid", "mixed", "first", "cell"])
+                    choices=["grid", "hybrid", "mixed", "first", "cell", "window"])
     ap.add_argument("--cell", default=None, help="Hq,Hkv,B,L,D,block_size for --workload cell")
     ap.add_argument("--no-curve", action="store_true", help="skip the steady-state curve")
     ap.add_argument("--seed", type=int, default=0)

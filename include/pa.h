@@ -74,6 +74,11 @@ typedef void* pa_stream_t; /* cudaStream_t */
  * Full argument set for pa_decode_ex. Fields beyond those of pa_decode:
  *   splits  0 = choose the split count automatically (fill every SM even at batch 1);
  *           > 0 = use at most this many splits of the context (tests, tuning).
+ *   window  0 = attend to the whole context; > 0 = sliding-window decode: each
+ *           query attends to the last `window` tokens of its context, t in
+ *           [max(0, L - window), L) (the sliding layers of "vLLM's custom ROCm
+ *           paged-attention kernel wins all sixty cells", section 4, scan 1024).
+ *           Table entries before the window are not read.
  * All other fields mean what the pa_decode parameters of the same name mean.
  */
 typedef struct pa_decode_args {
@@ -88,6 +93,7 @@ typedef struct pa_decode_args {
   float scale;
   int32_t dtype; /* pa_dtype */
   int32_t splits;
+  int32_t window;
 } pa_decode_args;
 
 /*

@@ -58,6 +58,7 @@ class DecodeArgs(ctypes.Structure):
         ("block_size", _c.c_int32), ("num_blocks", _c.c_int32),
         ("max_blocks_per_seq", _c.c_int32), ("max_seq_len", _c.c_int32),
         ("scale", _c.c_float), ("dtype", _c.c_int32), ("splits", _c.c_int32),
+        ("window", _c.c_int32),
     ]
 
 
@@ -116,7 +117,7 @@ def _stream_handle(device: torch.device, stream) -> int:
 
 
 def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
-              max_seq_len: Optional[int] = None, splits: int = 0) -> DecodeArgs:
+              max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0) -> DecodeArgs:
     """Check shapes / dtypes / devices and fill a pa_decode_args."""
     if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
         raise ValueError("q must be [B, Hq, D] and the caches [num_blocks, block_size, Hkv, D]")
@@ -151,6 +152,7 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     a.scale = float(scale)
     a.dtype = _DT[q.dtype]
     a.splits = int(splits)
+    a.window = int(window)
     return a
 
 
@@ -174,19 +176,22 @@ def workspace_for(args: DecodeArgs, device: torch.device, stream_handle: int) ->
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
            out: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
-           splits: int = 0, workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+           splits: int = 0, workspace: Optional[torch.Tensor] = None, stream=None,
+           window: int = 0) -> torch.Tensor:
     """out[b, h] = softmax(scale * q[b,h] . K_b^T) V_b over the paged context of sequence b.
 
     q [B, Hq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D]; block_tables
     [B, max_blocks] int32; seq_lens [B] int32; all on one CUDA device. max_seq_len
     bounds seq_lens (pass it: it sets the split plan; None means the table's
-    capacity). splits > 0 forces at most that many context splits. Asynchronous on
-    the current (or given) stream.
+    capacity). splits > 0 forces at most that many context splits. window > 0
+    attends to the last `window` tokens only. Asynchronous on the current (or given)
+    stream.
     """
     lib = load()
     if out is None:
         out = torch.empty_like(q)
-    args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, splits)
+    args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, splits,
+                     window)
     _ensure_device(lib, q.device.index)
     sh = _stream_handle(q.device, stream)
     ws = workspace if workspace is not None else workspace_for(args, q.device, sh)
@@ -236,7 +241,7 @@ def decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None,
 
 
 def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
-         splits: int = 0, sm_count: int = 0) -> Tuple[int, int]:
+         splits: int = 0, sm_count: int = 0, window: int = 0) -> Tuple[int, int]:
     """(splits, tokens per split) the library would launch with. sm_count <= 0 asks
     the current device; a positive sm_count needs no GPU."""
     lib = load()
@@ -247,6 +252,7 @@ def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
     a.max_seq_len = max_seq_len
     a.dtype = PA_BF16
     a.splits = splits
+    a.window = window
     S, P = ctypes.c_int(0), ctypes.c_int(0)
     rc = lib.pa_decode_plan(ctypes.byref(a), int(sm_count), ctypes.byref(S), ctypes.byref(P))
     if rc != PA_OK:

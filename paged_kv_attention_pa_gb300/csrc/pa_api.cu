@@ -125,7 +125,7 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   if (a->block_size <= 0 || a->num_blocks <= 0 || a->max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
   if (a->dtype != PA_F16 && a->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  if (a->splits < 0) return PA_ERR_INVALID_ARG;
+  if (a->splits < 0 || a->window < 0) return PA_ERR_INVALID_ARG;
   if (a->B > 65535 || a->Hkv > 65535) return PA_ERR_INVALID_ARG;  // grid limits
   // kernels address cache rows with 32-bit row indices
   if ((int64_t)a->num_blocks * a->block_size * a->Hkv > (int64_t)UINT32_MAX) return PA_ERR_UNSUPPORTED;
@@ -135,6 +135,11 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   if (ml > INT_MAX) return PA_ERR_OUT_OF_RANGE;
   *max_len = ml;
   return PA_OK;
+}
+
+// Tokens one sequence's splits must cover: a sliding window bounds them.
+int64_t plan_len(const pa_decode_args* a, int64_t max_len) {
+  return (a->window > 0 && a->window < max_len) ? a->window : max_len;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -174,7 +179,8 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
   if (sm_count <= 0) sm_count = current_sm_count();
   if (sm_count <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, max_len, a->splits, &plan))
+  if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
+                 &plan))
     return PA_ERR_UNSUPPORTED;
   *splits = plan.S;
   *partition_tokens = plan.P;
@@ -242,7 +248,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const int sm = current_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, max_len, a->splits, &plan))
+  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits, &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const WsLayout w = ws_layout(a->B, a->Hkv, G, a->D, plan.S);
@@ -270,6 +276,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.max_seq_len = (int)max_len;
   p.S = plan.S;
   p.P = plan.P;
+  p.window = a->window;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
 
   cudaStream_t cs = (cudaStream_t)stream;

@@ -82,7 +82,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool WIN>
 __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const DecodeParams p) {
   using C = Cfg<D, NT>;
   constexpr int GT = C::GT;
@@ -112,8 +112,22 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   // block-table entries of this warp's first tiles. Entries are read only inside
   // the table row; those past the sequence are ignored, never dereferenced.
   const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks;
-  const int t_begin = split * p.P;
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
+  int L = __ldg(p.seq_lens + b);
+  auto validate_len = [&]() {
+    if (L < 0 || L > cap) {
+      if (split == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
+      L = L < 0 ? 0 : cap;
+    }
+  };
+  // A sliding window starts the context at max(0, L - window): its splits depend on
+  // L, so only the full-context path requests the first table entries speculatively.
+  int t_lo = 0;
+  if constexpr (WIN) {
+    validate_len();
+    t_lo = max(0, L - p.window);
+  }
+  const int t_begin = t_lo + split * p.P;
   // block-table entry of token t0(k) + lane, for this warp's k-th tile
   auto table_entry = [&](int k) -> int {
     const long long t = (long long)t_begin + (long long)(warp + k * kWarps) * C::TW + lane;
@@ -123,7 +137,6 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   int pe[C::DEPTH];  // entries of tiles 0 .. DEPTH-1
 #pragma unroll
   for (int k = 0; k < C::DEPTH; ++k) pe[k] = table_entry(k);
-  int L = __ldg(p.seq_lens + b);
   // query fragments (B operand of the score MMA), unscaled, zero for padded heads
   uint32_t qf[NT][C::KS][2];
   {
@@ -142,10 +155,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   }
 
   // ---- context length, validated against the bounds the launch was planned for
-  if (L < 0 || L > cap) {
-    if (split == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
-    L = L < 0 ? 0 : cap;
-  }
+  if constexpr (!WIN) validate_len();
   if (L == 0) {  // empty context: a zero row, written once
     if (split == 0)
       for (int i = threadIdx.x; i < G * D; i += kThreads) out[head0 * D + i] = from_f32<T>(0.f);
@@ -154,7 +164,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
   if (t_begin >= L) return;  // this split lies past the sequence: nothing to do
   const int t_end = min(L, t_begin + p.P);
   const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
-  const int n_splits = (L + p.P - 1) / p.P;
+  const int n_splits = (L - t_lo + p.P - 1) / p.P;
 
   // ---- per-warp copy pipeline
   const uint64_t pol = l2_evict_first_policy();
@@ -374,6 +384,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   int L = __ldg(p.seq_lens + b);
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
   L = L < 0 ? 0 : (L > cap ? cap : L);
+  if (p.window > 0) L = min(L, p.window);  // tokens the splits cover
   const int n = (L + p.P - 1) / p.P;
   if (n <= 1) return;  // written by the decode grid
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
@@ -454,7 +465,7 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool WIN>
 cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
   using C = Cfg<D, NT>;
   // The dynamic shared memory opt-in is per device; remember which devices have it.
@@ -464,12 +475,12 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<T, D, NT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  e = launch_pdl(decode_kernel<T, D, NT>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
+  e = launch_pdl(decode_kernel<T, D, NT, WIN>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
   if (e != cudaSuccess) return e;
   if (p.S > 1) e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq, p.B), dim3(256), 0, st, p);
   return e;
@@ -477,7 +488,9 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
 
 template <typename T, int D>
 cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st) {
-  return p.G <= 8 ? launch_decode_nt<T, D, 1>(p, st) : launch_decode_nt<T, D, 2>(p, st);
+  if (p.window > 0)
+    return p.G <= 8 ? launch_decode_nt<T, D, 1, true>(p, st) : launch_decode_nt<T, D, 2, true>(p, st);
+  return p.G <= 8 ? launch_decode_nt<T, D, 1, false>(p, st) : launch_decode_nt<T, D, 2, false>(p, st);
 }
 
 }  // namespace pa

@@ -33,6 +33,7 @@ struct DecodeParams {
   int B, Hq, Hkv, G;
   int block_size, num_blocks, max_blocks, max_seq_len;
   int S, P;           // splits and tokens per split
+  int window;         // > 0: attend to the last `window` tokens only
   float scale_log2;   // scale * log2(e): scores live in the exp2 domain
 };
 

@@ -28,12 +28,12 @@ def read_golden(name: str):
     return rows
 
 
-def oracle_case(case: PagedCase) -> np.ndarray:
+def oracle_case(case: PagedCase, window: int = 0) -> np.ndarray:
     """Float64 oracle output for a whole case, from its contiguous K/V."""
     q = to_f64_numpy(case.q)
     K = [to_f64_numpy(k) for k in case.K]
     V = [to_f64_numpy(v) for v in case.V]
-    return decode_ref(q, K, V, case.scale)
+    return decode_ref(q, K, V, case.scale, window=window)
 
 
 def oracle_rows(case: PagedCase, pairs: Iterable[tuple]) -> dict:

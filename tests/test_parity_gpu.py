@@ -300,6 +300,49 @@ def test_cuda_graph_replay(cuda_lib):
     assert torch.equal(out, ref)
 
 
+# ------------------------------------------------------------------ sliding window
+@pytest.mark.parametrize("W", [1, 16, 1000, 1024, 4096])
+def test_sliding_window(cuda_lib, W):
+    lens = [500, 1024, 1025, 4097, 9000]
+    case = pi.make_case(5, 16, 8, 128, 16, lens, seed=50 + W, poison="kv_nan").to("cuda")
+    y = run(cuda_lib, case, window=W)
+    assert_parity(to_np(y), oracle_case(case, window=W), what=f"window {W}")
+    no_device_errors(cuda_lib)
+
+
+@pytest.mark.parametrize("L", [800, 5000, 32768])
+def test_sliding_window_hybrid(cuda_lib, L):
+    case = pi.make_case(1, 24, 4, 256, 784, [L], seed=L + 7, poison="v_nan")
+    y = run(cuda_lib, case, window=1024)
+    assert_parity(to_np(y), oracle_case(case, window=1024), what=f"hybrid window L={L}")
+
+
+def test_window_never_attends_before_its_start(cuda_lib):
+    # keys before the window get a huge score: attending to any of them would swamp
+    # the output; the windowed result must match the oracle over the window alone
+    W, L = 512, 3001
+    case = pi.make_case(1, 8, 8, 128, 16, [L], seed=60)
+    q = case.q[0].double()
+    for h in range(8):
+        case.K[0][: L - W, h] = (30.0 / case.scale * q[h] / (q[h] @ q[h])).to(case.K[0].dtype)
+    bt = case.block_tables[0].long()
+    t = torch.arange(L)
+    case.k_cache[bt[t // 16], t % 16] = case.K[0]
+    ref = oracle_case(case, window=W)
+    y = run(cuda_lib, case, window=W)
+    assert_parity(to_np(y), ref, what="window start")
+    full = oracle_case(case)
+    assert np.abs(full - ref).max() > 0.1 * np.abs(ref).max()   # the planted keys matter
+
+
+@pytest.mark.parametrize("S", [1, 3, 7, 64])
+def test_sliding_window_forced_splits(cuda_lib, S):
+    case = pi.make_case(3, 32, 8, 128, 16, [2049, 700, 5000], seed=61).to("cuda")
+    ref = oracle_case(case, window=1536)
+    y = run(cuda_lib, case, splits=S, window=1536)
+    assert_parity(to_np(y), ref, what=f"window splits={S}")
+
+
 # ------------------------------------------------------------------ device-side errors
 def test_bad_block_index_is_reported_not_faulted(cuda_lib):
     case = pi.make_case(1, 8, 8, 128, 16, [100], seed=22).to("cuda")
