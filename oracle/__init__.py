@@ -9,5 +9,6 @@ from the paged cache, as the page "vLLM's custom ROCm paged-attention kernel
 wins all sixty cells" (gqa-gate-costs-nothing, §1) does for its reference.
 """
 from .decode_ref import decode_ref, decode_ref_one, rel_linf_error
+from .fp8 import dequant, e4m3_to_float64
 
-__all__ = ["decode_ref", "decode_ref_one", "rel_linf_error"]
+__all__ = ["decode_ref", "decode_ref_one", "rel_linf_error", "dequant", "e4m3_to_float64"]

@@ -37,6 +37,8 @@ import torch
 POISON_MODES = ("none", "k_nan", "v_nan", "kv_nan", "kv_1e4", "kv_inf")
 
 _DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16}
+FP8 = torch.float8_e4m3fn
+FP8_SCALE = 8.0 / 448.0   # default per-tensor scale: N(0,1) values to 8 sigma fit e4m3
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -59,6 +61,12 @@ class PagedCase:
     dtype: str
     poison: str = "none"
     meta: dict = field(default_factory=dict)
+    k_scale: float = 1.0            # cache element = stored value * scale (fp8 caches)
+    v_scale: float = 1.0
+
+    @property
+    def kv_fp8(self) -> bool:
+        return self.k_cache.dtype == FP8
 
     @property
     def B(self) -> int:
@@ -89,7 +97,7 @@ class PagedCase:
         return PagedCase(mv(self.q), [mv(k) for k in self.K], [mv(v) for v in self.V],
                          mv(self.k_cache), mv(self.v_cache), mv(self.block_tables),
                          mv(self.seq_lens), self.scale, self.block_size, self.dtype,
-                         self.poison, dict(self.meta))
+                         self.poison, dict(self.meta), self.k_scale, self.v_scale)
 
 
 def fp32_scale(D: int) -> float:
@@ -143,7 +151,8 @@ def make_case(B: int, Hq: int, Hkv: int, D: int, block_size: int,
               pool_factor: float = 2.0, num_blocks: Optional[int] = None,
               poison: str = "none", table_fill: str = "neg1",
               device: str = "cpu", scale: Optional[float] = None,
-              max_blocks: Optional[int] = None) -> PagedCase:
+              max_blocks: Optional[int] = None, kv_dtype: Optional[str] = None,
+              k_scale: float = FP8_SCALE, v_scale: float = FP8_SCALE) -> PagedCase:
     """Build one seeded decode call.
 
     ``seq_lens`` gives L_b per sequence. The pool holds ``pool_factor`` times the
@@ -152,6 +161,8 @@ def make_case(B: int, Hq: int, Hkv: int, D: int, block_size: int,
     sequences interleave. Table entries past a sequence's last block are filled with
     -1 (``table_fill='neg1'``) or with an index past the pool (``'oob'``): a correct
     kernel never reads them. ``device='cuda'`` draws on the GPU (large cases).
+    ``kv_dtype='fp8'`` stores K/V as FP8 E4M3 codes of value / scale (per-tensor
+    k_scale, v_scale, rounded to fp32); K[b], V[b] then hold those codes too.
     """
     assert len(seq_lens) == B
     assert Hq % Hkv == 0
@@ -177,15 +188,27 @@ def make_case(B: int, Hq: int, Hkv: int, D: int, block_size: int,
         perm = None
 
     q = rnd((B, Hq, D))
-    K = [rnd((L, Hkv, D)) for L in seq_lens]
-    V = [rnd((L, Hkv, D)) for L in seq_lens]
+    fp8 = kv_dtype == "fp8"
+    k_scale = float(np.float32(k_scale)) if fp8 else 1.0
+    v_scale = float(np.float32(v_scale)) if fp8 else 1.0
+    if fp8:  # draw in the q dtype, then quantise value / scale to e4m3
+        K = [(rnd((L, Hkv, D)).float() / k_scale).to(FP8) for L in seq_lens]
+        V = [(rnd((L, Hkv, D)).float() / v_scale).to(FP8) for L in seq_lens]
+        cdt = FP8
+    else:
+        K = [rnd((L, Hkv, D)) for L in seq_lens]
+        V = [rnd((L, Hkv, D)) for L in seq_lens]
+        cdt = tdt
     if perm is None:
         perm = torch.from_numpy(rng.permutation(num_blocks).astype(np.int64))
 
-    k_cache = torch.zeros((num_blocks, bs, Hkv, D), dtype=tdt, device=device)
+    k_cache = torch.zeros((num_blocks, bs, Hkv, D), dtype=cdt, device=device)
     v_cache = torch.zeros_like(k_cache)
-    kfill = _fill_values(poison, "k", tdt)
-    vfill = _fill_values(poison, "v", tdt)
+    kfill = _fill_values(poison, "k", cdt)
+    vfill = _fill_values(poison, "v", cdt)
+    if fp8:  # e4m3 has no infinity and tops out at 448: finite garbage saturates there
+        kfill = None if kfill is None else (448.0 if np.isfinite(kfill) else float("nan"))
+        vfill = None if vfill is None else (448.0 if np.isfinite(vfill) else float("nan"))
     if kfill is not None:
         k_cache.fill_(kfill)
     if vfill is not None:
@@ -211,7 +234,8 @@ def make_case(B: int, Hq: int, Hkv: int, D: int, block_size: int,
                      block_tables=bt.to(torch.int32), seq_lens=sl,
                      scale=fp32_scale(D) if scale is None else float(np.float32(scale)),
                      block_size=bs, dtype=dtype, poison=poison,
-                     meta={"seed": seed, "num_blocks": num_blocks, "used_blocks": used})
+                     meta={"seed": seed, "num_blocks": num_blocks, "used_blocks": used},
+                     k_scale=k_scale, v_scale=v_scale)
 
 
 def gather_back(case: PagedCase, b: int):
@@ -236,6 +260,9 @@ def repage(case: PagedCase, seed: int) -> PagedCase:
     # same way, then scatter the tokens at their new homes.
     kf = _fill_values(case.poison, "k", k_cache.dtype)
     vf = _fill_values(case.poison, "v", v_cache.dtype)
+    if k_cache.dtype == FP8:
+        kf = None if kf is None else (448.0 if np.isfinite(kf) else float("nan"))
+        vf = None if vf is None else (448.0 if np.isfinite(vf) else float("nan"))
     k_cache.fill_(0.0 if kf is None else kf)
     v_cache.fill_(0.0 if vf is None else vf)
     bt = case.block_tables.clone().to(torch.int64)
@@ -251,9 +278,15 @@ def repage(case: PagedCase, seed: int) -> PagedCase:
         k_cache[bt[b, t // bs], t % bs] = case.K[b]
         v_cache[bt[b, t // bs], t % bs] = case.V[b]
     return PagedCase(case.q, case.K, case.V, k_cache, v_cache, bt.to(torch.int32),
-                     case.seq_lens, case.scale, bs, case.dtype, case.poison, dict(case.meta))
+                     case.seq_lens, case.scale, bs, case.dtype, case.poison, dict(case.meta),
+                     case.k_scale, case.v_scale)
 
 
 def to_f64_numpy(t: torch.Tensor) -> np.ndarray:
     """Exact widening of an fp16/bf16 tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def fp8_codes(t: torch.Tensor) -> np.ndarray:
+    """The raw uint8 codes of an FP8 E4M3 tensor (for the oracle's own decoder)."""
+    return t.detach().to("cpu").view(torch.uint8).numpy()

@@ -7,7 +7,8 @@ from typing import Iterable, Optional
 import numpy as np
 
 from oracle import decode_ref, decode_ref_one, rel_linf_error
-from pa_inputs import PagedCase, to_f64_numpy
+from oracle import dequant
+from pa_inputs import PagedCase, fp8_codes, to_f64_numpy
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -28,11 +29,19 @@ def read_golden(name: str):
     return rows
 
 
+def kv_f64(case: PagedCase, t, which: str) -> np.ndarray:
+    """Contiguous K or V of one sequence as float64 cache values (fp8 decoded by the
+    oracle's own E4M3 decoder and scaled)."""
+    if case.kv_fp8:
+        return dequant(fp8_codes(t), case.k_scale if which == "k" else case.v_scale)
+    return to_f64_numpy(t)
+
+
 def oracle_case(case: PagedCase, window: int = 0) -> np.ndarray:
     """Float64 oracle output for a whole case, from its contiguous K/V."""
     q = to_f64_numpy(case.q)
-    K = [to_f64_numpy(k) for k in case.K]
-    V = [to_f64_numpy(v) for v in case.V]
+    K = [kv_f64(case, k, "k") for k in case.K]
+    V = [kv_f64(case, v, "v") for v in case.V]
     return decode_ref(q, K, V, case.scale, window=window)
 
 
@@ -42,8 +51,8 @@ def oracle_rows(case: PagedCase, pairs: Iterable[tuple]) -> dict:
     out = {}
     for b, kvh in pairs:
         qg = to_f64_numpy(case.q[b, kvh * G:(kvh + 1) * G])
-        K = to_f64_numpy(case.K[b][:, kvh, :])
-        V = to_f64_numpy(case.V[b][:, kvh, :])
+        K = kv_f64(case, case.K[b][:, kvh, :], "k")
+        V = kv_f64(case, case.V[b][:, kvh, :], "v")
         out[(b, kvh)] = decode_ref_one(qg, K, V, case.scale)
     return out
 

@@ -102,3 +102,17 @@ def test_uniform_seq_lens_range():
     lens = pi.uniform_seq_lens(64, 1024, 32768, seed=0)
     assert len(lens) == 64 and min(lens) >= 1024 and max(lens) <= 32768
     assert any(L % 16 for L in lens), "not block-aligned"
+
+
+def test_fp8_case_roundtrip_and_fills():
+    from harness import kv_f64
+    case = pi.make_case(2, 8, 4, 16, 16, [37, 5], seed=70, kv_dtype="fp8", poison="kv_nan")
+    assert case.k_cache.dtype == pi.FP8 and case.kv_fp8
+    for b in range(2):
+        k, v = pi.gather_back(case, b)
+        assert torch.equal(k.view(torch.uint8), case.K[b].view(torch.uint8))
+    kf = kv_f64(case, case.K[0], "k")
+    # quantisation error of value / scale -> e4m3 is at most half an ulp (2^-4 relative)
+    q = pi.make_case(2, 8, 4, 16, 16, [37, 5], seed=70)  # same draws, unquantised
+    ref = q.K[0].double().numpy()
+    assert np.all(np.abs(kf - ref) <= 2.0 ** -4 * np.abs(ref) + 2.0 ** -9 * case.k_scale)
