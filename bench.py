@@ -52,6 +52,8 @@ GRID_BATCHES = [1, 8]
 HYBRID_LENS = [500, 1024, 2048, 4096, 8192, 12288, 16384, 20480, 24576, 28672, 32768]
 FALLBACK_HBM_GBS = 6800.0
 ROTATE_BYTES = 512 << 20  # KV per rotation of the steady-state curve (4x the 129 MB L2)
+FP8_SCALE = 8.0 / 448.0   # per-tensor scale of the fp8 caches (N(0,1) to 8 sigma)
+KV_FP8 = False            # set by --kv-dtype fp8
 
 
 # ---------------------------------------------------------------------- workloads
@@ -59,10 +61,13 @@ class Inst:
     """One set of device inputs for a decode call."""
 
     def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, exact,
-                 window=0):
+                 window=0, fp8=False):
         gen = torch.Generator(device=device)
         gen.manual_seed(seed)
         dt = torch.bfloat16
+        cdt = torch.float8_e4m3fn if fp8 else dt
+        # fp8 caches: stored value = N(0,1) draw / FP8_SCALE (rounded to e4m3)
+        cv = (lambda x: (x.float() / FP8_SCALE).to(cdt)) if fp8 else (lambda x: x.to(dt))
         nblk = [-(-L // bs) for L in lens]
         # timing copies of a windowed call back only the blocks the window can touch;
         # earlier logical blocks share them (they are never read)
@@ -73,12 +78,12 @@ class Inst:
         if exact:
             # live tokens N(0,1); spare blocks and unwritten tails keep the fill
             fill = float("nan") if poison == "nan" else 0.0
-            self.k = torch.full((nb, bs, Hkv, D), fill, dtype=dt, device=device)
-            self.v = torch.full((nb, bs, Hkv, D), fill, dtype=dt, device=device)
+            self.k = torch.full((nb, bs, Hkv, D), fill, dtype=cdt, device=device)
+            self.v = torch.full((nb, bs, Hkv, D), fill, dtype=cdt, device=device)
         else:
             # timing copies: the whole pool N(0,1) (values do not change the work)
-            self.k = torch.randn((nb, bs, Hkv, D), generator=gen, device=device).to(dt)
-            self.v = torch.randn((nb, bs, Hkv, D), generator=gen, device=device).to(dt)
+            self.k = cv(torch.randn((nb, bs, Hkv, D), generator=gen, device=device))
+            self.v = cv(torch.randn((nb, bs, Hkv, D), generator=gen, device=device))
         perm = torch.randperm(nb, generator=gen, device=device)
         bt = torch.full((B, max(nblk)), -1, dtype=torch.int32, device=device)
         off = 0
@@ -93,8 +98,8 @@ class Inst:
             if exact:
                 t = torch.arange(L, device=device)
                 phys = bt[b, (t // bs)].long()
-                self.k[phys, t % bs] = torch.randn((L, Hkv, D), generator=gen, device=device).to(dt)
-                self.v[phys, t % bs] = torch.randn((L, Hkv, D), generator=gen, device=device).to(dt)
+                self.k[phys, t % bs] = cv(torch.randn((L, Hkv, D), generator=gen, device=device))
+                self.v[phys, t % bs] = cv(torch.randn((L, Hkv, D), generator=gen, device=device))
         self.bt = bt
         self.sl = torch.tensor(lens, dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
@@ -104,13 +109,16 @@ class Cell:
     """A decode configuration: inputs for the step, plus copies for the curve."""
 
     def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison=None, pool_factor=2.0,
-                 tag="", window=0):
+                 tag="", window=0, fp8=None):
         self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
         self.window = window
+        self.fp8 = KV_FP8 if fp8 is None else fp8
+        self.kv_elem = 1 if self.fp8 else 2
         self.lens = list(lens)
         self.tag = tag
         self.seed, self.device, self.poison, self.pool_factor = seed, device, poison, pool_factor
-        self.insts = [Inst(B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, True)]
+        self.insts = [Inst(B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, True,
+                           window, self.fp8)]
         self.max_len = max(lens)
         self.scale = float(np.float32(1.0 / math.sqrt(D)))
         self.ws = None
@@ -119,14 +127,14 @@ class Cell:
         for i in range(len(self.insts), n):
             self.insts.append(Inst(self.B, self.Hq, self.Hkv, self.D, self.bs, self.lens,
                                    self.seed + 7919 * i, self.device, self.poison,
-                                   self.pool_factor, False, self.window))
+                                   self.pool_factor, False, self.window, self.fp8))
 
     def read_lens(self):
         """Tokens each sequence's query attends to (the window bounds them)."""
         return [min(L, self.window) if self.window > 0 else L for L in self.lens]
 
     def kv_bytes(self) -> int:
-        return sum(self.read_lens()) * self.Hkv * self.D * 2 * 2
+        return sum(self.read_lens()) * self.Hkv * self.D * 2 * self.kv_elem
 
     def alg_bytes(self) -> int:
         """Bytes the method must move: KV, the live block-table entries, q, out, seq_lens."""
@@ -136,7 +144,8 @@ class Cell:
     def call(self, pa, stream=None, i=0):
         x = self.insts[i]
         pa.decode(x.q, x.k, x.v, x.bt, x.sl, self.scale, out=x.out, max_seq_len=self.max_len,
-                  workspace=self.ws, stream=stream, window=self.window)
+                  workspace=self.ws, stream=stream, window=self.window,
+                  k_scale=FP8_SCALE, v_scale=FP8_SCALE)
 
 
 def parse_cell(spec):
@@ -395,7 +404,8 @@ def run_ours(args, rank, world, local_rank):
     # one workspace per cell so the captured graph has fixed addresses
     for c in cells:
         x = c.insts[0]
-        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len, 0, c.window)
+        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len, 0, c.window,
+                         FP8_SCALE, FP8_SCALE)
         nbytes = lib.pa_decode_ex_workspace_bytes(ctypes.byref(a))
         c.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -518,9 +528,11 @@ def run_ours(args, rank, world, local_rank):
         "impl": "ours", "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step_max, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16 q/out, fp8-e4m3 KV" if KV_FP8 else "bf16",
+        "data": "synthetic",
         "config": dict(desc, **{
             "parallelism": f"replicas{world}" if world > 1 else "single",
+            "kv_dtype": "fp8_e4m3" if KV_FP8 else "bf16",
             "l2": "inputs larger than L2: each step reads every cell's own cache once "
                   f"({kv / 2**30:.2f} GiB of distinct KV per step)",
             "timed": "CUDA graph of the whole step, replayed K times, CUDA events",
@@ -561,7 +573,11 @@ def main():
     ap.add_argument("--cell", default=None, help="Hq,Hkv,B,L,D,block_size for --workload cell")
     ap.add_argument("--no-curve", action="store_true", help="skip the steady-state curve")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="cache element type (fp8 = E4M3 with a per-tensor scale)")
     args = ap.parse_args()
+    global KV_FP8
+    KV_FP8 = args.kv_dtype == "fp8"
     if args.warmup < 3:
         args.warmup = 3
 

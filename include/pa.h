@@ -60,6 +60,13 @@ typedef enum pa_status {
 
 typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 
+/* Element type of the K/V caches in pa_decode_args.kv_dtype. */
+typedef enum pa_kv_dtype {
+  PA_KV_AS_DTYPE = 0, /* the caches have the q/out dtype */
+  PA_KV_FP8_E4M3 = 1  /* FP8 E4M3 ("fn": bias 7, no infinities, max 448), one byte per
+                         element; cache value = stored value * k_scale (K) or v_scale (V) */
+} pa_kv_dtype;
+
 /* Bits of the device error word (workspace header). */
 #define PA_DEVERR_BLOCK_INDEX 1u /* a live token's block table entry was outside [0, num_blocks) */
 #define PA_DEVERR_SEQ_LEN 2u     /* a seq_len < 0, > max_seq_len or > max_blocks_per_seq*block_size */
@@ -79,6 +86,14 @@ typedef void* pa_stream_t; /* cudaStream_t */
  *           [max(0, L - window), L) (the sliding layers of "vLLM's custom ROCm
  *           paged-attention kernel wins all sixty cells", section 4, scan 1024).
  *           Table entries before the window are not read.
+ *   kv_dtype  PA_KV_AS_DTYPE (default) or PA_KV_FP8_E4M3: the caches hold one byte
+ *           per element, [num_blocks, block_size, Hkv, D] as before; q and out keep
+ *           `dtype`. fp8 K/V are widened exactly to fp16 for the tensor-core
+ *           products (the queries are rounded to fp16, P is kept in fp16) with fp32
+ *           accumulation. The pages list an fp8 cache as untested ("vLLM's custom
+ *           ROCm paged-attention kernel wins all sixty cells", section 6).
+ *   k_scale, v_scale  per-tensor dequantisation scales (finite, > 0) for an fp8
+ *           cache; ignored otherwise.
  * All other fields mean what the pa_decode parameters of the same name mean.
  */
 typedef struct pa_decode_args {
@@ -94,6 +109,8 @@ typedef struct pa_decode_args {
   int32_t dtype; /* pa_dtype */
   int32_t splits;
   int32_t window;
+  int32_t kv_dtype; /* pa_kv_dtype */
+  float k_scale, v_scale;
 } pa_decode_args;
 
 /*

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_PKG, "libpa.so")
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, \
     PA_ERR_OUT_OF_RANGE = range(6)
 PA_F16, PA_BF16 = 0, 1
+PA_KV_AS_DTYPE, PA_KV_FP8_E4M3 = 0, 1
 PA_DEVERR_BLOCK_INDEX, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT = 1, 2, 4
 MAX_GQA_GROUP = 16
 
@@ -58,7 +59,8 @@ class DecodeArgs(ctypes.Structure):
         ("block_size", _c.c_int32), ("num_blocks", _c.c_int32),
         ("max_blocks_per_seq", _c.c_int32), ("max_seq_len", _c.c_int32),
         ("scale", _c.c_float), ("dtype", _c.c_int32), ("splits", _c.c_int32),
-        ("window", _c.c_int32),
+        ("window", _c.c_int32), ("kv_dtype", _c.c_int32),
+        ("k_scale", _c.c_float), ("v_scale", _c.c_float),
     ]
 
 
@@ -117,7 +119,8 @@ def _stream_handle(device: torch.device, stream) -> int:
 
 
 def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
-              max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0) -> DecodeArgs:
+              max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0,
+              k_scale: float = 1.0, v_scale: float = 1.0) -> DecodeArgs:
     """Check shapes / dtypes / devices and fill a pa_decode_args."""
     if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
         raise ValueError("q must be [B, Hq, D] and the caches [num_blocks, block_size, Hkv, D]")
@@ -125,9 +128,11 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     nb, bs, Hkv, Dk = k_cache.shape
     if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
         raise ValueError("k_cache / v_cache / q shapes disagree")
-    if q.dtype not in _DT or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype or \
-            out.dtype != q.dtype:
-        raise TypeError("q, k_cache, v_cache and out must share one dtype: float16 or bfloat16")
+    fp8 = k_cache.dtype == torch.float8_e4m3fn
+    if q.dtype not in _DT or out.dtype != q.dtype or v_cache.dtype != k_cache.dtype or \
+            (k_cache.dtype != q.dtype and not fp8):
+        raise TypeError("q and out must be float16 or bfloat16; the caches must have their "
+                        "dtype or both be float8_e4m3fn")
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(seq_lens.shape) != (B,):
@@ -153,6 +158,8 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     a.dtype = _DT[q.dtype]
     a.splits = int(splits)
     a.window = int(window)
+    a.kv_dtype = PA_KV_FP8_E4M3 if fp8 else PA_KV_AS_DTYPE
+    a.k_scale, a.v_scale = (float(k_scale), float(v_scale)) if fp8 else (1.0, 1.0)
     return a
 
 
@@ -177,21 +184,21 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
            out: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
            splits: int = 0, workspace: Optional[torch.Tensor] = None, stream=None,
-           window: int = 0) -> torch.Tensor:
+           window: int = 0, k_scale: float = 1.0, v_scale: float = 1.0) -> torch.Tensor:
     """out[b, h] = softmax(scale * q[b,h] . K_b^T) V_b over the paged context of sequence b.
 
     q [B, Hq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D]; block_tables
     [B, max_blocks] int32; seq_lens [B] int32; all on one CUDA device. max_seq_len
     bounds seq_lens (pass it: it sets the split plan; None means the table's
     capacity). splits > 0 forces at most that many context splits. window > 0
-    attends to the last `window` tokens only. Asynchronous on the current (or given)
-    stream.
+    attends to the last `window` tokens only. float8_e4m3fn caches are read as
+    stored value * k_scale / v_scale. Asynchronous on the current (or given) stream.
     """
     lib = load()
     if out is None:
         out = torch.empty_like(q)
     args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, splits,
-                     window)
+                     window, k_scale, v_scale)
     _ensure_device(lib, q.device.index)
     sh = _stream_handle(q.device, stream)
     ws = workspace if workspace is not None else workspace_for(args, q.device, sh)

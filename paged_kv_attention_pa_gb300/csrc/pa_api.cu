@@ -126,6 +126,10 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
     return PA_ERR_INVALID_ARG;
   if (a->dtype != PA_F16 && a->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (a->splits < 0 || a->window < 0) return PA_ERR_INVALID_ARG;
+  if (a->kv_dtype != PA_KV_AS_DTYPE && a->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (a->kv_dtype == PA_KV_FP8_E4M3 &&
+      !(a->k_scale > 0.f && a->v_scale > 0.f && a->k_scale < INFINITY && a->v_scale < INFINITY))
+    return PA_ERR_INVALID_ARG;
   if (a->B > 65535 || a->Hkv > 65535) return PA_ERR_INVALID_ARG;  // grid limits
   // kernels address cache rows with 32-bit row indices
   if ((int64_t)a->num_blocks * a->block_size * a->Hkv > (int64_t)UINT32_MAX) return PA_ERR_UNSUPPORTED;
@@ -277,15 +281,24 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.S = plan.S;
   p.P = plan.P;
   p.window = a->window;
-  p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+  p.kv_fp8 = a->kv_dtype == PA_KV_FP8_E4M3;
+  p.v_scale = p.kv_fp8 ? a->v_scale : 1.f;
+  // scores live in the exp2 domain; an fp8 K's scale multiplies every score
+  p.scale_log2 = (float)((double)a->scale * 1.4426950408889634 * (p.kv_fp8 ? (double)a->k_scale : 1.0));
 
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e;
   const bool bf16 = a->dtype == PA_BF16;
-  if (a->D == 128)
+  if (p.kv_fp8) {
+    if (a->D == 128)
+      e = bf16 ? pa::launch_decode_fp8_bf16_d128(p, cs) : pa::launch_decode_fp8_f16_d128(p, cs);
+    else
+      e = bf16 ? pa::launch_decode_fp8_bf16_d256(p, cs) : pa::launch_decode_fp8_f16_d256(p, cs);
+  } else if (a->D == 128) {
     e = bf16 ? pa::launch_decode_bf16_d128(p, cs) : pa::launch_decode_f16_d128(p, cs);
-  else
+  } else {
     e = bf16 ? pa::launch_decode_bf16_d256(p, cs) : pa::launch_decode_f16_d256(p, cs);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PA_ERR_CUDA;

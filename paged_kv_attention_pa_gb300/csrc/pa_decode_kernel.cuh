@@ -30,6 +30,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "pa.h"
 #include "pa_device.cuh"
@@ -47,26 +48,31 @@ namespace pa {
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kTileTokens = 16;  // M of the score MMA
 
-template <int D, int NT>
+// F8: the cache holds FP8 E4M3 (one byte per element); tiles land in the ring as
+// bytes and each warp widens its tile into an fp16 staging tile for the MMAs.
+template <int D, int NT, bool F8 = false>
 struct Cfg {
   static constexpr int NW = D == 128 ? PA_WARPS_D128 : PA_WARPS_D256;  // warps per CTA
   static constexpr int THREADS = NW * 32;
   static constexpr int TW = kTileTokens;
   static constexpr int GT = 8 * NT;             // heads computed (G padded)
-  static constexpr int ROWB = D * 2 + 16;       // smem row pitch, padded against bank conflicts
-  static constexpr int CPR = D * 2 / 16;        // 16-byte chunks per row
+  static constexpr int KVB = F8 ? 1 : 2;        // bytes per cache element
+  static constexpr int ROWB = D * KVB + 16;     // ring row pitch, padded against bank conflicts
+  static constexpr int ROWB_M = D * 2 + 16;     // MMA-operand row pitch (16-bit elements)
+  static constexpr int CPR = D * KVB / 16;      // 16-byte chunks per row
   static constexpr int TILE_BYTES = TW * ROWB;  // K (or V) half of a slot
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
+  static constexpr int STAGE_BYTES = F8 ? TW * ROWB_M : 0;  // per warp, V only (fp8 only)
   static constexpr int KS = D / 16;             // k-steps of the score MMA = d-blocks of PV
   static constexpr int COPIES = TW * CPR / 32;  // 16-byte copies per lane per operand per tile
   static constexpr int FIXED = 256;
-  static constexpr int DEPTH_FIT = (kSmemBudget - FIXED) / (NW * SLOT_BYTES);
+  static constexpr int DEPTH_FIT = (kSmemBudget - FIXED - NW * STAGE_BYTES) / (NW * SLOT_BYTES);
   static constexpr int DEPTH = DEPTH_FIT > 12 ? 12 : DEPTH_FIT;  // slots per warp
   static constexpr int RING = NW * DEPTH * SLOT_BYTES;
-  static constexpr int SMEM = RING + FIXED;
+  static constexpr int SMEM = RING + NW * STAGE_BYTES + FIXED;
   static_assert((TW * CPR) % 32 == 0, "tile shape");
   static_assert(DEPTH >= 2, "need at least two slots per warp");
-  static_assert(NW * GT * (D + 2) * 4 <= RING, "CTA merge must fit in the ring");
+  static_assert(NW * GT * (D + 2) * 4 <= RING + NW * STAGE_BYTES, "CTA merge must fit");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
@@ -82,9 +88,13 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename T, int D, int NT, bool WIN>
-__global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const DecodeParams p) {
-  using C = Cfg<D, NT>;
+// T: q and out type; KV: cache element type (T, or fp8e4m3 with fp16 MMAs).
+template <typename T, typename KV, int D, int NT, bool WIN>
+__global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREADS, 1)
+    decode_kernel(const DecodeParams p) {
+  constexpr bool F8 = std::is_same_v<KV, fp8e4m3>;
+  using TM = std::conditional_t<F8, __half, T>;  // MMA operand type
+  using C = Cfg<D, NT, F8>;
   constexpr int GT = C::GT;
   constexpr int kWarps = C::NW;
   constexpr int kThreads = C::THREADS;
@@ -148,8 +158,18 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
       const size_t rowp = ((head0 + (ok ? g : 0)) * D) / 2;  // in bf16/f16 pairs
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk) {
-        qf[nt][kk][0] = ok ? __ldg(q32 + rowp + kk * 8 + tig) : 0u;
-        qf[nt][kk][1] = ok ? __ldg(q32 + rowp + kk * 8 + 4 + tig) : 0u;
+        // fp8 caches feed K to the MMA in a permuted d order: fragment elements
+        // {2tig, 2tig+1, 2tig+8, 2tig+9} of k-step kk hold d = 16kk + 4tig + {0,1,2,3};
+        // q takes the same order, so every dot product is unchanged.
+        const int i0 = F8 ? kk * 8 + 2 * tig : kk * 8 + tig;
+        const int i1 = F8 ? kk * 8 + 2 * tig + 1 : kk * 8 + 4 + tig;
+        qf[nt][kk][0] = ok ? __ldg(q32 + rowp + i0) : 0u;
+        qf[nt][kk][1] = ok ? __ldg(q32 + rowp + i1) : 0u;
+        if constexpr (F8 && !std::is_same_v<T, __half>) {  // queries as fp16 pairs
+          const float2 a0 = unpack2<T>(qf[nt][kk][0]), a1 = unpack2<T>(qf[nt][kk][1]);
+          qf[nt][kk][0] = pack2<__half>(a0.x, a0.y);
+          qf[nt][kk][1] = pack2<__half>(a1.x, a1.y);
+        }
       }
     }
   }
@@ -201,7 +221,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
         const int r = flat / C::CPR, c = flat % C::CPR;
         const uint32_t rr = __shfl_sync(0xffffffffu, ridx, r);
         if (r < nv) {
-          const uint8_t* src = kbase + (size_t)rr * (D * 2) + c * 16;
+          const uint8_t* src = kbase + (size_t)rr * (D * C::KVB) + c * 16;
           const uint32_t dst = slot + r * C::ROWB + c * 16;
           cp_async16(dst, src, pol);
           cp_async16(dst + C::TILE_BYTES, src + v_minus_k, pol);
@@ -226,8 +246,9 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
     for (int dd = 0; dd < C::KS; ++dd) o[nt][dd][0] = o[nt][dd][1] = o[nt][dd][2] = o[nt][dd][3] = 0.f;
   }
   // ldmatrix row addresses (byte offsets inside a tile) for this lane
-  const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB + (lane >> 4) * 16);
-  const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB + ((lane >> 3) & 1) * 16);
+  const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB_M + (lane >> 4) * 16);
+  const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB_M + ((lane >> 3) & 1) * 16);
+  uint8_t* my_stage = ring + C::RING + warp * C::STAGE_BYTES;  // fp8 only
   const float sl2 = p.scale_log2;
 
   for (int k = 0; k < my_tiles; ++k) {
@@ -237,29 +258,82 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
     cp_async_wait<C::DEPTH - 1>();  // tile k has landed (for this lane's copies)
     const int j = warp + k * kWarps;
     const int nv = min(C::TW, t_end - (t_begin + j * C::TW));
-    const uint32_t kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
-    const uint32_t vt = kt + C::TILE_BYTES;
-    if (nv < C::TW) {
-      // rows past seq_len were never loaded: zero them in V so that p = 0 meets 0
-      uint8_t* vrow = my_ring + (k % C::DEPTH) * C::SLOT_BYTES + C::TILE_BYTES;
-      for (int i = lane; i < (C::TW - nv) * C::CPR; i += 32) {
-        const int r = nv + i / C::CPR, c = i % C::CPR;
-        *reinterpret_cast<uint4*>(vrow + r * C::ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t kt, vt;
+    if constexpr (F8) {
+      // widen this tile's V bytes to fp16 in the warp's staging tile (the PV MMA reads
+      // V transposed); rows past seq_len (never loaded) become zeros, so that p = 0
+      // meets 0 in the PV sum. K stays in the ring: the score MMA widens it in
+      // registers.
+      __syncwarp();  // every lane's copies have landed
+      const uint8_t* slot = my_ring + (k % C::DEPTH) * C::SLOT_BYTES;
+#pragma unroll
+      for (int i = 0; i < C::COPIES; ++i) {
+        const int flat = i * 32 + lane;
+        const int r = flat / C::CPR, c = flat % C::CPR;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if (r < nv) {
+          const uint4 w = *reinterpret_cast<const uint4*>(slot + C::TILE_BYTES + r * C::ROWB + c * 16);
+          lo = make_uint4(e4m3x2_to_half2(w.x & 0xffff), e4m3x2_to_half2(w.x >> 16),
+                          e4m3x2_to_half2(w.y & 0xffff), e4m3x2_to_half2(w.y >> 16));
+          hi = make_uint4(e4m3x2_to_half2(w.z & 0xffff), e4m3x2_to_half2(w.z >> 16),
+                          e4m3x2_to_half2(w.w & 0xffff), e4m3x2_to_half2(w.w >> 16));
+        }
+        uint8_t* dst = my_stage + r * C::ROWB_M + c * 32;
+        *reinterpret_cast<uint4*>(dst) = lo;
+        *reinterpret_cast<uint4*>(dst + 16) = hi;
+      }
+      kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
+      vt = smem_addr(my_stage);
+    } else {
+      kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
+      vt = kt + C::TILE_BYTES;
+      if (nv < C::TW) {
+        // rows past seq_len were never loaded: zero them in V so that p = 0 meets 0
+        uint8_t* vrow = my_ring + (k % C::DEPTH) * C::SLOT_BYTES + C::TILE_BYTES;
+        for (int i = lane; i < (C::TW - nv) * C::CPR; i += 32) {
+          const int r = nv + i / C::CPR, c = i % C::CPR;
+          *reinterpret_cast<uint4*>(vrow + r * C::ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     __syncwarp();  // every lane's copies (and the zero rows) are visible
 
     // ---- scores S^T[token][head] = K_tile . q^T (fp32 accumulate)
-    float s[NT][4];
+    // two independent accumulator chains (even / odd k-steps) halve the MMA latency
+    float s[NT][4], s2[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < C::KS; ++kk) {
       uint32_t a[4];
-      ldmatrix_x4<false>(a, kt + k_lane + kk * 32);
+      if constexpr (F8) {
+        // rows gid and gid + 8, d = 16kk + 4tig .. +3: four e4m3 bytes each
+        uint32_t w0, w1;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(kt + gid * C::ROWB + kk * 16 + 4 * tig));
+        asm volatile("ld.shared.u32 %0, [%1];"
+                     : "=r"(w1)
+                     : "r"(kt + (gid + 8) * C::ROWB + kk * 16 + 4 * tig));
+        a[0] = e4m3x2_to_half2(w0 & 0xffff);
+        a[2] = e4m3x2_to_half2(w0 >> 16);
+        a[1] = e4m3x2_to_half2(w1 & 0xffff);
+        a[3] = e4m3x2_to_half2(w1 >> 16);
+      } else {
+        ldmatrix_x4<false>(a, kt + k_lane + kk * 32);
+      }
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<T>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        if (kk & 1)
+          mma16816<TM>(s2[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        else
+          mma16816<TM>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+      }
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
     // rows gid and gid + 8 of the tile; -inf by select past seq_len
     const bool live0 = gid < nv, live1 = gid + 8 < nv;
     uint32_t pb[NT][2];
@@ -293,8 +367,8 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
         o[nt][dd][3] *= al1;
       }
       // P^T[token][head] fragments -> P[head][token] as the B operand of PV
-      pb[nt][0] = movmatrix_trans(pack2<T>(p0, p1));
-      pb[nt][1] = movmatrix_trans(pack2<T>(p2, p3));
+      pb[nt][0] = movmatrix_trans(pack2<TM>(p0, p1));
+      pb[nt][1] = movmatrix_trans(pack2<TM>(p2, p3));
     }
 
     // ---- O^T[d][head] += V_tile^T . P^T
@@ -303,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
       uint32_t a[4];
       ldmatrix_x4<true>(a, vt + v_lane + dd * 32);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][dd], a, pb[nt][0], pb[nt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma16816<TM>(o[nt][dd], a, pb[nt][0], pb[nt][1]);
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
   }
@@ -356,6 +430,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::THREADS, 1) decode_kernel(const De
       num += e * aw[(w * GT + g) * D + d];
       den += e * lw[w * GT + g];
     }
+    num *= p.v_scale;  // cache values are stored values times v_scale (1 unless fp8)
     if (single) {
       out[(head0 + g) * D + d] = from_f32<T>(num / den);
     } else {
@@ -465,9 +540,9 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename T, int D, int NT, bool WIN>
+template <typename T, typename KV, int D, int NT, bool WIN>
 cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
-  using C = Cfg<D, NT>;
+  using C = Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>;
   // The dynamic shared memory opt-in is per device; remember which devices have it.
   static unsigned long long done_mask = 0ull;
   int dev = 0;
@@ -475,22 +550,24 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_kernel<T, D, NT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<T, KV, D, NT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  e = launch_pdl(decode_kernel<T, D, NT, WIN>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
+  e = launch_pdl(decode_kernel<T, KV, D, NT, WIN>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
   if (e != cudaSuccess) return e;
   if (p.S > 1) e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq, p.B), dim3(256), 0, st, p);
   return e;
 }
 
-template <typename T, int D>
+template <typename T, typename KV, int D>
 cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st) {
   if (p.window > 0)
-    return p.G <= 8 ? launch_decode_nt<T, D, 1, true>(p, st) : launch_decode_nt<T, D, 2, true>(p, st);
-  return p.G <= 8 ? launch_decode_nt<T, D, 1, false>(p, st) : launch_decode_nt<T, D, 2, false>(p, st);
+    return p.G <= 8 ? launch_decode_nt<T, KV, D, 1, true>(p, st)
+                    : launch_decode_nt<T, KV, D, 2, true>(p, st);
+  return p.G <= 8 ? launch_decode_nt<T, KV, D, 1, false>(p, st)
+                  : launch_decode_nt<T, KV, D, 2, false>(p, st);
 }
 
 }  // namespace pa

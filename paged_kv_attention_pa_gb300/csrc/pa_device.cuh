@@ -20,6 +20,21 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// ---------------------------------------------------------------- fp8 caches
+// Tag type of an FP8 E4M3 cache element (one byte: sign, 4-bit exponent with bias
+// 7, 3-bit mantissa; no infinities).
+struct fp8e4m3 {
+  uint8_t bits;
+};
+
+// Two E4M3 values (low byte = element 0) to a packed pair of fp16, exactly: every
+// E4M3 value is representable in fp16.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
+  uint32_t y;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- dependent launch
 // Wait until the grids this one depends on (programmatic launch) have completed
 // and their writes are visible; returns at once for an ordinary launch.

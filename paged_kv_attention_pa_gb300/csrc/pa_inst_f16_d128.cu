@@ -1,8 +1,8 @@
-// Decode kernels for f16 caches with head_dim 128, one per GQA group size.
+// Decode kernels for f16 caches with head_dim 128.
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
 cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st) {
-  return launch_decode_dispatch<__half, 128>(p, st);
+  return launch_decode_dispatch<__half, __half, 128>(p, st);
 }
 }  // namespace pa

@@ -1,8 +1,8 @@
-// Decode kernels for f16 caches with head_dim 256, one per GQA group size.
+// Decode kernels for f16 caches with head_dim 256.
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
 cudaError_t launch_decode_f16_d256(const DecodeParams& p, cudaStream_t st) {
-  return launch_decode_dispatch<__half, 256>(p, st);
+  return launch_decode_dispatch<__half, __half, 256>(p, st);
 }
 }  // namespace pa

@@ -1,0 +1,8 @@
+// Decode kernels for FP8 E4M3 caches with f16 queries, head_dim 256.
+#include "pa_decode_kernel.cuh"
+
+namespace pa {
+cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st) {
+  return launch_decode_dispatch<__half, fp8e4m3, 256>(p, st);
+}
+}  // namespace pa

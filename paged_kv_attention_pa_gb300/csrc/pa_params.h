@@ -34,6 +34,8 @@ struct DecodeParams {
   int block_size, num_blocks, max_blocks, max_seq_len;
   int S, P;           // splits and tokens per split
   int window;         // > 0: attend to the last `window` tokens only
+  int kv_fp8;         // caches hold FP8 E4M3 (k_scale is folded into scale_log2)
+  float v_scale;      // cache V value = stored value * v_scale
   float scale_log2;   // scale * log2(e): scores live in the exp2 domain
 };
 
@@ -42,5 +44,10 @@ cudaError_t launch_decode_bf16_d128(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_decode_bf16_d256(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_decode_f16_d256(const DecodeParams& p, cudaStream_t st);
+// FP8 E4M3 caches with bf16 / fp16 queries and outputs.
+cudaError_t launch_decode_fp8_bf16_d128(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_fp8_bf16_d256(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_fp8_f16_d128(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st);
 
 }  // namespace pa

@@ -70,6 +70,10 @@ def _call(lib, a, ws=256, nbytes=1 << 20):
     (dict(out=0), pa.PA_ERR_INVALID_ARG),
     (dict(k_cache=40), pa.PA_ERR_INVALID_ARG),              # not 16-byte aligned
     (dict(num_blocks=1 << 24, block_size=784, Hkv=8, Hq=8), pa.PA_ERR_UNSUPPORTED),  # rows > 2^32
+    (dict(kv_dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(kv_dtype=pa.PA_KV_FP8_E4M3, k_scale=0.0, v_scale=1.0), pa.PA_ERR_INVALID_ARG),
+    (dict(kv_dtype=pa.PA_KV_FP8_E4M3, k_scale=1.0, v_scale=float("inf")), pa.PA_ERR_INVALID_ARG),
+    (dict(window=-1), pa.PA_ERR_INVALID_ARG),
 ])
 def test_host_validation(lib, kw, code):
     assert _call(lib, _args(**kw)) == code

@@ -23,6 +23,9 @@ GRID_SHAPES = [(8, 8), (16, 8), (24, 8), (32, 8), (32, 16)]
 
 def run(pa, case, **kw):
     c = case if case.q.is_cuda else case.to("cuda")
+    if c.kv_fp8:
+        kw.setdefault("k_scale", c.k_scale)
+        kw.setdefault("v_scale", c.v_scale)
     out = pa.decode(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
                     max_seq_len=kw.pop("max_seq_len", c.max_seq_len), **kw)
     torch.cuda.synchronize()
@@ -341,6 +344,53 @@ def test_sliding_window_forced_splits(cuda_lib, S):
     ref = oracle_case(case, window=1536)
     y = run(cuda_lib, case, splits=S, window=1536)
     assert_parity(to_np(y), ref, what=f"window splits={S}")
+
+
+# ------------------------------------------------------------------ fp8 KV cache
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8)])
+def test_fp8_cache_poison_matrix(cuda_lib, dtype, hq, hkv):
+    lens = [1023, 4097]
+    outs = {}
+    for mode in pi.POISON_MODES:
+        case = pi.make_case(2, hq, hkv, 128, 16, lens, dtype=dtype, seed=80, poison=mode,
+                            kv_dtype="fp8")
+        y = run(cuda_lib, case)
+        if mode == "none":
+            ref = oracle_case(case)
+        assert_parity(to_np(y), ref, what=f"fp8 {mode} {dtype} {hq}/{hkv}")
+        outs[mode] = y
+    for mode, y in outs.items():
+        assert torch.equal(y, outs["none"]), f"fp8 output depends on the {mode} fill"
+    no_device_errors(cuda_lib)
+
+
+@pytest.mark.parametrize("L", [500, 5000, 32768])
+def test_fp8_cache_hybrid(cuda_lib, L):
+    case = pi.make_case(1, 24, 4, 256, 784, [L], seed=81, kv_dtype="fp8", poison="v_nan")
+    assert_parity(to_np(run(cuda_lib, case)), oracle_case(case), what=f"fp8 hybrid L={L}")
+
+
+def test_fp8_cache_scales_window_and_splits(cuda_lib):
+    case = pi.make_case(3, 32, 16, 128, 16, [3000, 77, 6001], seed=82, kv_dtype="fp8",
+                        k_scale=0.03, v_scale=0.05).to("cuda")
+    assert_parity(to_np(run(cuda_lib, case)), oracle_case(case), what="fp8 scales")
+    for S in (1, 5):
+        assert_parity(to_np(run(cuda_lib, case, splits=S)), oracle_case(case),
+                      what=f"fp8 splits={S}")
+    assert_parity(to_np(run(cuda_lib, case, window=1024)), oracle_case(case, window=1024),
+                  what="fp8 window")
+
+
+def test_fp8_cache_mixed_batch_sampled(cuda_lib):
+    lens = pi.uniform_seq_lens(64, 1024, 32768, seed=3)
+    case = pi.make_case(64, 32, 8, 128, 16, lens, seed=83, pool_factor=1.1, poison="kv_nan",
+                        device="cuda", kv_dtype="fp8")
+    y = run(cuda_lib, case)
+    assert torch.isfinite(y).all()
+    rng = random.Random(3)
+    pairs = sorted({(rng.randrange(64), rng.randrange(8)) for _ in range(8)})
+    check_sampled(cuda_lib, case, y, pairs, "fp8 mixed batch")
 
 
 # ------------------------------------------------------------------ device-side errors
