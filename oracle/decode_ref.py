@@ -96,3 +96,30 @@ def rel_linf_error(y: np.ndarray, r: np.ndarray) -> float:
     num = float(np.max(np.abs(y - r))) if y.size else 0.0
     den = float(np.max(np.abs(r))) if r.size else 0.0
     return num / den if den > 0.0 else num
+
+
+def decode_ref_rows(q: np.ndarray, K_list: Sequence[np.ndarray], V_list: Sequence[np.ndarray],
+                    scale: float) -> np.ndarray:
+    """Decode with several query rows per sequence, causal among the new rows.
+
+    q: [B, R, Hq, D] float64: the queries of the last R tokens of each context
+    (speculative-decode rows, or the tail of a chunked prefill; "vLLM's custom ROCm
+    paged-attention kernel wins all sixty cells", §6, names speculation that makes
+    decode carry several query rows). Row i of sequence b is the query of token
+    L_b - R + i and attends to the tokens t < L_b - R + i + 1: every earlier token
+    and itself. A row left with no tokens (L_b < R - i) gives zeros. Each row is
+    the single-row definition over its own prefix of K/V. Returns [B, R, Hq, D].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, R, Hq, D = q.shape
+    out = np.zeros((B, R, Hq, D), dtype=np.float64)
+    for b in range(B):
+        K = np.asarray(K_list[b], dtype=np.float64)
+        V = np.asarray(V_list[b], dtype=np.float64)
+        L = K.shape[0]
+        for i in range(R):
+            lim = L - R + i + 1
+            if lim <= 0:
+                continue
+            out[b, i] = decode_ref(q[b, i][None], [K[:lim]], [V[:lim]], scale)[0]
+    return out

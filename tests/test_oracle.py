@@ -316,3 +316,57 @@ def test_window_pins_catch_off_by_one():
     wrong = decode_ref(q, [k[1:] for k in K], [v[1:] for v in V], scale, window=W - 1)
     r = _brute_force_decimal(q, [k[-W:] for k in K], [v[-W:] for v in V], scale)
     assert np.abs(wrong - r).max() > 1e-6
+
+
+# ----------------------------------------------------------------- several query rows
+from oracle import decode_ref_rows
+
+
+def test_rows_one_row_is_decode():
+    q, K, V, scale = _rand_problem(44, lens=(7, 3))
+    y = decode_ref_rows(q[:, None], K, V, scale)
+    assert np.array_equal(y[:, 0], decode_ref(q, K, V, scale))
+
+
+def test_rows_brute_force_causal():
+    # brute force each row over exactly the tokens up to its own position
+    rng = np.random.Generator(np.random.PCG64(45))
+    B, R, Hq, Hkv, D = 2, 3, 4, 2, 4
+    lens = (6, 4)
+    q = rng.standard_normal((B, R, Hq, D))
+    K = [rng.standard_normal((L, Hkv, D)) for L in lens]
+    V = [rng.standard_normal((L, Hkv, D)) for L in lens]
+    y = decode_ref_rows(q, K, V, 0.5)
+    for b, L in enumerate(lens):
+        for i in range(R):
+            lim = L - R + i + 1
+            r = _brute_force_decimal(q[b, i][None], [K[b][:lim]], [V[b][:lim]], 0.5)
+            assert np.abs(y[b, i] - r[0]).max() <= 1e-14 * max(1.0, np.abs(r).max())
+
+
+def test_rows_causality():
+    # changing token t only changes the rows that can see it
+    rng = np.random.Generator(np.random.PCG64(46))
+    B, R, L = 1, 4, 9
+    q = rng.standard_normal((B, R, 2, 4))
+    K = [rng.standard_normal((L, 1, 4))]
+    V = [rng.standard_normal((L, 1, 4))]
+    y = decode_ref_rows(q, K, V, 0.7)
+    t = L - 2                      # visible to rows 2 and 3 only
+    K2 = [K[0].copy()]
+    V2 = [V[0].copy()]
+    K2[0][t] += 3.0
+    V2[0][t] -= 5.0
+    y2 = decode_ref_rows(q, K2, V2, 0.7)
+    assert np.array_equal(y[0, :2], y2[0, :2])
+    assert np.abs(y[0, 2:] - y2[0, 2:]).min() > 0
+
+
+def test_rows_short_context_gives_zero_rows():
+    rng = np.random.Generator(np.random.PCG64(47))
+    q = rng.standard_normal((1, 4, 2, 4))
+    K = [rng.standard_normal((2, 1, 4))]
+    V = [rng.standard_normal((2, 1, 4))]
+    y = decode_ref_rows(q, K, V, 1.0)
+    assert np.all(y[0, :2] == 0) and np.all(np.isfinite(y))
+    assert np.array_equal(y[0, 2, 0], V[0][0, 0])   # row 2 sees one token
