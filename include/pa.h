@@ -94,6 +94,13 @@ typedef void* pa_stream_t; /* cudaStream_t */
  *           ROCm paged-attention kernel wins all sixty cells", section 6).
  *   k_scale, v_scale  per-tensor dequantisation scales (finite, > 0) for an fp8
  *           cache; ignored otherwise.
+ *   q_len   query rows per sequence (0 or 1 = single-query decode). With R > 1 rows,
+ *           q and out are [B, R, Hq, D]: row i is the query of token L - R + i (the
+ *           new tokens of a speculative-decode step or a chunked-prefill tail) and
+ *           attends causally to the tokens t < L - R + i + 1; a row that sees no
+ *           token gets zeros. Every K/V tile is read once for all rows and heads of
+ *           its KV head. Limits: G * R <= 32 at head_dim 128, <= 16 at 256; not
+ *           combined with a window (PA_ERR_UNSUPPORTED).
  * All other fields mean what the pa_decode parameters of the same name mean.
  */
 typedef struct pa_decode_args {
@@ -111,6 +118,7 @@ typedef struct pa_decode_args {
   int32_t window;
   int32_t kv_dtype; /* pa_kv_dtype */
   float k_scale, v_scale;
+  int32_t q_len;
 } pa_decode_args;
 
 /*

@@ -60,7 +60,7 @@ class DecodeArgs(ctypes.Structure):
         ("max_blocks_per_seq", _c.c_int32), ("max_seq_len", _c.c_int32),
         ("scale", _c.c_float), ("dtype", _c.c_int32), ("splits", _c.c_int32),
         ("window", _c.c_int32), ("kv_dtype", _c.c_int32),
-        ("k_scale", _c.c_float), ("v_scale", _c.c_float),
+        ("k_scale", _c.c_float), ("v_scale", _c.c_float), ("q_len", _c.c_int32),
     ]
 
 
@@ -121,10 +121,15 @@ def _stream_handle(device: torch.device, stream) -> int:
 def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
               max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0,
               k_scale: float = 1.0, v_scale: float = 1.0) -> DecodeArgs:
-    """Check shapes / dtypes / devices and fill a pa_decode_args."""
-    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
-        raise ValueError("q must be [B, Hq, D] and the caches [num_blocks, block_size, Hkv, D]")
-    B, Hq, D = q.shape
+    """Check shapes / dtypes / devices and fill a pa_decode_args. q is [B, Hq, D], or
+    [B, R, Hq, D] for R causal query rows per sequence."""
+    if q.dim() not in (3, 4) or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, D] or [B, R, Hq, D] and the caches "
+                         "[num_blocks, block_size, Hkv, D]")
+    if q.dim() == 4:
+        B, R, Hq, D = q.shape
+    else:
+        (B, Hq, D), R = q.shape, 1
     nb, bs, Hkv, Dk = k_cache.shape
     if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
         raise ValueError("k_cache / v_cache / q shapes disagree")
@@ -158,6 +163,7 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     a.dtype = _DT[q.dtype]
     a.splits = int(splits)
     a.window = int(window)
+    a.q_len = R
     a.kv_dtype = PA_KV_FP8_E4M3 if fp8 else PA_KV_AS_DTYPE
     a.k_scale, a.v_scale = (float(k_scale), float(v_scale)) if fp8 else (1.0, 1.0)
     return a

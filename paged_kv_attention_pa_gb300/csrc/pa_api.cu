@@ -125,7 +125,14 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   if (a->block_size <= 0 || a->num_blocks <= 0 || a->max_blocks_per_seq <= 0)
     return PA_ERR_INVALID_ARG;
   if (a->dtype != PA_F16 && a->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  if (a->splits < 0 || a->window < 0) return PA_ERR_INVALID_ARG;
+  if (a->splits < 0 || a->window < 0 || a->q_len < 0) return PA_ERR_INVALID_ARG;
+  {
+    const int64_t rows = a->q_len > 0 ? a->q_len : 1;
+    const int64_t cols = (int64_t)(a->Hq / a->Hkv) * rows;
+    if (rows > 1 && a->window > 0) return PA_ERR_UNSUPPORTED;        // one or the other
+    if (cols > (a->D == 128 ? 32 : 16)) return PA_ERR_UNSUPPORTED;    // (rows x group) per CTA
+    if ((int64_t)a->Hq * rows > 65535) return PA_ERR_INVALID_ARG;     // merge grid limit
+  }
   if (a->kv_dtype != PA_KV_AS_DTYPE && a->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
   if (a->kv_dtype == PA_KV_FP8_E4M3 &&
       !(a->k_scale > 0.f && a->v_scale > 0.f && a->k_scale < INFINITY && a->v_scale < INFINITY))
@@ -194,7 +201,8 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
 size_t pa_decode_ex_workspace_bytes(const pa_decode_args* a) {
   int S = 0, P = 0;
   if (pa_decode_plan(a, 0, &S, &P) != PA_OK) return 0;
-  return ws_layout(a->B, a->Hkv, a->Hq / a->Hkv, a->D, S).total;
+  const int rows = a->q_len > 0 ? a->q_len : 1;
+  return ws_layout(a->B, a->Hkv, (int64_t)(a->Hq / a->Hkv) * rows, a->D, S).total;
 }
 
 size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size,
@@ -255,7 +263,8 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits, &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
-  const WsLayout w = ws_layout(a->B, a->Hkv, G, a->D, plan.S);
+  const int rows = a->q_len > 0 ? a->q_len : 1;
+  const WsLayout w = ws_layout(a->B, a->Hkv, (int64_t)G * rows, a->D, plan.S);
   if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -281,6 +290,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.S = plan.S;
   p.P = plan.P;
   p.window = a->window;
+  p.q_len = rows;
   p.kv_fp8 = a->kv_dtype == PA_KV_FP8_E4M3;
   p.v_scale = p.kv_fp8 ? a->v_scale : 1.f;
   // scores live in the exp2 domain; an fp8 K's scale multiplies every score

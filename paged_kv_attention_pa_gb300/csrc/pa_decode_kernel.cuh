@@ -109,8 +109,12 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   const int gid = lane >> 2;  // fragment row group
   const int tig = lane & 3;   // thread in group
   const int G = p.G;
+  const int R = p.q_len;   // query rows per sequence (1 for single-query decode)
+  const int cols = G * R;  // MMA columns: column c is (row c / G, head kvh*G + c % G)
   T* out = reinterpret_cast<T*>(p.out);
-  const size_t head0 = (size_t)b * p.Hq + (size_t)kvh * G;
+  auto qrow = [&](int c) -> size_t {  // row of q / out holding column c
+    return ((size_t)b * R + c / G) * p.Hq + (size_t)kvh * G + c % G;
+  };
 
   // Inputs may come from the previous kernel in the stream: wait for it (a no-op
   // without a programmatic launch), then let the merge grid get scheduled.
@@ -153,9 +157,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + gid;
-      const bool ok = g < G;
-      const size_t rowp = ((head0 + (ok ? g : 0)) * D) / 2;  // in bf16/f16 pairs
+      const int c = nt * 8 + gid;
+      const bool ok = c < cols;
+      const size_t rowp = (qrow(ok ? c : 0) * D) / 2;  // in bf16/f16 pairs
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk) {
         // fp8 caches feed K to the MMA in a permuted d order: fragment elements
@@ -176,15 +180,23 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 
   // ---- context length, validated against the bounds the launch was planned for
   if constexpr (!WIN) validate_len();
-  if (L == 0) {  // empty context: a zero row, written once
+  if (L == 0) {  // empty context: zero rows, written once
     if (split == 0)
-      for (int i = threadIdx.x; i < G * D; i += kThreads) out[head0 * D + i] = from_f32<T>(0.f);
+      for (int i = threadIdx.x; i < cols * D; i += kThreads)
+        out[qrow(i / D) * D + i % D] = from_f32<T>(0.f);
     return;
   }
   if (t_begin >= L) return;  // this split lies past the sequence: nothing to do
   const int t_end = min(L, t_begin + p.P);
   const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
   const int n_splits = (L - t_lo + p.P - 1) / p.P;
+  // Causal limit of each of this thread's columns: row i sees tokens t < L - R + i + 1
+  // (all of them when R = 1), and this split only its own tokens t < t_end.
+  int lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) lim[nt][h] = min(t_end, L - R + (nt * 8 + 2 * tig + h) / G + 1);
 
   // ---- per-warp copy pipeline
   const uint64_t pol = l2_evict_first_policy();
@@ -334,15 +346,16 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
-    // rows gid and gid + 8 of the tile; -inf by select past seq_len
-    const bool live0 = gid < nv, live1 = gid + 8 < nv;
+    // tokens gid and gid + 8 of the tile; -inf by select past each column's limit
+    // (seq_len, this split's end, and the causal limit of the column's query row)
+    const int tok0 = t_begin + j * C::TW + gid, tok1 = tok0 + 8;
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float x0 = live0 ? s[nt][0] * sl2 : -INFINITY;
-      float x1 = live0 ? s[nt][1] * sl2 : -INFINITY;
-      float x2 = live1 ? s[nt][2] * sl2 : -INFINITY;
-      float x3 = live1 ? s[nt][3] * sl2 : -INFINITY;
+      float x0 = tok0 < lim[nt][0] ? s[nt][0] * sl2 : -INFINITY;
+      float x1 = tok0 < lim[nt][1] ? s[nt][1] * sl2 : -INFINITY;
+      float x2 = tok1 < lim[nt][0] ? s[nt][2] * sl2 : -INFINITY;
+      float x3 = tok1 < lim[nt][1] ? s[nt][3] * sl2 : -INFINITY;
       // tile max per head over the 16 tokens (lanes sharing tig)
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
@@ -418,26 +431,28 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 
   const bool single = n_splits == 1;
   const size_t pidx = ((size_t)b * p.Hkv + kvh) * p.S + split;
-  for (int i = threadIdx.x; i < G * D; i += kThreads) {
-    const int g = i / D, d = i - (i / D) * D;
+  for (int i = threadIdx.x; i < cols * D; i += kThreads) {
+    const int g = i / D, d = i - (i / D) * D;  // g: column
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GT + g]);
     float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {  // a column whose row sees no token of this split stays empty
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float e = exp2f(mw[w * GT + g] - M);  // idle warps: m = -inf, weight 0
-      num += e * aw[(w * GT + g) * D + d];
-      den += e * lw[w * GT + g];
+      for (int w = 0; w < kWarps; ++w) {
+        const float e = exp2f(mw[w * GT + g] - M);  // idle warps: m = -inf, weight 0
+        num += e * aw[(w * GT + g) * D + d];
+        den += e * lw[w * GT + g];
+      }
     }
     num *= p.v_scale;  // cache values are stored values times v_scale (1 unless fp8)
     if (single) {
-      out[(head0 + g) * D + d] = from_f32<T>(num / den);
+      out[qrow(g) * D + d] = from_f32<T>(den > 0.f ? num / den : 0.f);
     } else {
-      p.ws_acc[(pidx * G + g) * D + d] = num;
+      p.ws_acc[(pidx * cols + g) * D + d] = num;
       if (d == 0) {
-        p.ws_m[pidx * G + g] = M;
-        p.ws_l[pidx * G + g] = den;
+        p.ws_m[pidx * cols + g] = M;
+        p.ws_l[pidx * cols + g] = den;
       }
     }
   }
@@ -445,8 +460,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 
 // Combine the split partials of one (sequence, query head, 64-wide slice of D):
 //   M = max_s m_s,  w_s = 2^(m_s - M),  out = sum_s w_s acc_s / sum_s w_s l_s
-// (the flash-decoding reduction). Every split holds at least one live token, so
-// m_s is finite and the weights are well defined. 256 threads: 64 output
+// (the flash-decoding reduction). Splits where a row sees no token carry m = -inf
+// and weight 0. M is finite whenever the row sees a token; a row that sees none
+// (several query rows, short context) is written as zeros. 256 threads: 64 output
 // elements x 4 split lanes.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
@@ -454,8 +470,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   pdl_launch_dependents();
   __shared__ float ms[kMaxSplits], ws[kMaxSplits];
   __shared__ float red[8], part[4][64];
-  const int b = blockIdx.z, h = blockIdx.y;
+  const int b = blockIdx.z, row = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
   const int G = p.G, kvh = h / G, g = h - kvh * G;
+  const int cols = G * p.q_len, c = row * G + g;  // the partials' column of (row, head)
   int L = __ldg(p.seq_lens + b);
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
   L = L < 0 ? 0 : (L > cap ? cap : L);
@@ -466,7 +483,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int dl = tid & 63, sl = tid >> 6;
   const int d = blockIdx.x * 64 + dl;
-  const float* acc = p.ws_acc + (base * G + g) * D + d;
+  const float* acc = p.ws_acc + (base * cols + c) * D + d;
 
   // The accumulators do not depend on the weights: request the first 16 splits of
   // this thread's lane together with the maxima and sums (one round trip).
@@ -475,14 +492,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
     const int s2 = sl + 4 * i;
-    av[i] = s2 < n ? __ldcg(acc + (size_t)s2 * G * D) : 0.f;
+    av[i] = s2 < n ? __ldcg(acc + (size_t)s2 * cols * D) : 0.f;
   }
 
   float mx = -INFINITY;
   for (int s2 = tid; s2 < n; s2 += 256) {
-    const float v = __ldcg(p.ws_m + (base + s2) * G + g);
+    const float v = __ldcg(p.ws_m + (base + s2) * cols + c);
     ms[s2] = v;
-    ws[s2] = __ldcg(p.ws_l + (base + s2) * G + g);
+    ws[s2] = __ldcg(p.ws_l + (base + s2) * cols + c);
     mx = fmaxf(mx, v);
   }
   for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -494,7 +511,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   __syncthreads();
   float den = 0.f;
   for (int s2 = tid; s2 < n; s2 += 256) {
-    const float w = exp2f(ms[s2] - M);
+    const float w = M == -INFINITY ? 0.f : exp2f(ms[s2] - M);
     den += w * ws[s2];
     ms[s2] = w;  // ms now holds the weights
   }
@@ -512,12 +529,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
     if (s2 < n) num += ms[s2] * av[i];
   }
 #pragma unroll 8
-  for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * G * D);
+  for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * cols * D);
   part[sl][dl] = num;
   __syncthreads();
   if (sl == 0) {
     num = part[0][dl] + part[1][dl] + part[2][dl] + part[3][dl];
-    reinterpret_cast<T*>(p.out)[((size_t)b * p.Hq + h) * D + d] = from_f32<T>(num / den);
+    reinterpret_cast<T*>(p.out)[(((size_t)b * p.q_len + row) * p.Hq + h) * D + d] =
+        from_f32<T>(den > 0.f ? num / den : 0.f);
   }
 }
 
@@ -557,17 +575,23 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
   }
   e = launch_pdl(decode_kernel<T, KV, D, NT, WIN>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
   if (e != cudaSuccess) return e;
-  if (p.S > 1) e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq, p.B), dim3(256), 0, st, p);
+  if (p.S > 1)
+    e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq * p.q_len, p.B), dim3(256), 0, st, p);
   return e;
 }
 
+// Column tiles of 8: one for up to 8 (row, head) columns, two for 16, four for 32
+// (head_dim 128 only, no window: the host rejects the rest).
 template <typename T, typename KV, int D>
 cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st) {
+  const int cols = p.G * p.q_len;
   if (p.window > 0)
-    return p.G <= 8 ? launch_decode_nt<T, KV, D, 1, true>(p, st)
-                    : launch_decode_nt<T, KV, D, 2, true>(p, st);
-  return p.G <= 8 ? launch_decode_nt<T, KV, D, 1, false>(p, st)
-                  : launch_decode_nt<T, KV, D, 2, false>(p, st);
+    return cols <= 8 ? launch_decode_nt<T, KV, D, 1, true>(p, st)
+                     : launch_decode_nt<T, KV, D, 2, true>(p, st);
+  if (cols <= 8) return launch_decode_nt<T, KV, D, 1, false>(p, st);
+  if (cols <= 16 || D != 128) return launch_decode_nt<T, KV, D, 2, false>(p, st);
+  if constexpr (D == 128) return launch_decode_nt<T, KV, D, 4, false>(p, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

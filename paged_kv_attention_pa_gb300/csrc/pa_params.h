@@ -34,6 +34,7 @@ struct DecodeParams {
   int block_size, num_blocks, max_blocks, max_seq_len;
   int S, P;           // splits and tokens per split
   int window;         // > 0: attend to the last `window` tokens only
+  int q_len;          // query rows per sequence (causal among themselves)
   int kv_fp8;         // caches hold FP8 E4M3 (k_scale is folded into scale_log2)
   float v_scale;      // cache V value = stored value * v_scale
   float scale_log2;   // scale * log2(e): scores live in the exp2 domain

@@ -7,7 +7,7 @@ from typing import Iterable, Optional
 import numpy as np
 
 from oracle import decode_ref, decode_ref_one, rel_linf_error
-from oracle import dequant
+from oracle import decode_ref_rows, dequant
 from pa_inputs import PagedCase, fp8_codes, to_f64_numpy
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -69,3 +69,11 @@ def assert_parity(y: np.ndarray, r: np.ndarray, tol: float = REL_LINF_TOL, what:
 def kv_bytes(seq_lens, Hkv: int, D: int, elem_bytes: int = 2) -> int:
     """KV bytes one decode call must read: sum_b L_b * Hkv * D * 2 (K and V) * elem."""
     return int(sum(int(L) for L in seq_lens)) * Hkv * D * 2 * elem_bytes
+
+
+def oracle_rows_case(case: PagedCase) -> np.ndarray:
+    """Float64 oracle for a case whose q is [B, R, Hq, D] (causal query rows)."""
+    q = to_f64_numpy(case.q)
+    K = [kv_f64(case, k, "k") for k in case.K]
+    V = [kv_f64(case, v, "v") for v in case.V]
+    return decode_ref_rows(q, K, V, case.scale)

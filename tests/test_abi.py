@@ -74,6 +74,10 @@ def _call(lib, a, ws=256, nbytes=1 << 20):
     (dict(kv_dtype=pa.PA_KV_FP8_E4M3, k_scale=0.0, v_scale=1.0), pa.PA_ERR_INVALID_ARG),
     (dict(kv_dtype=pa.PA_KV_FP8_E4M3, k_scale=1.0, v_scale=float("inf")), pa.PA_ERR_INVALID_ARG),
     (dict(window=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(q_len=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(q_len=2, window=64), pa.PA_ERR_UNSUPPORTED),      # rows and a window: not both
+    (dict(q_len=5, Hq=56, Hkv=8), pa.PA_ERR_UNSUPPORTED),   # 7 x 5 = 35 columns > 32
+    (dict(q_len=3, Hq=48, Hkv=8, D=256), pa.PA_ERR_UNSUPPORTED),  # 18 columns > 16
 ])
 def test_host_validation(lib, kw, code):
     assert _call(lib, _args(**kw)) == code

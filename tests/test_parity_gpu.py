@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import pa_inputs as pi
-from harness import assert_parity, oracle_case, oracle_rows, read_golden
+from harness import assert_parity, oracle_case, oracle_rows, oracle_rows_case, read_golden
 
 pytestmark = pytest.mark.gpu
 
@@ -391,6 +391,53 @@ def test_fp8_cache_mixed_batch_sampled(cuda_lib):
     rng = random.Random(3)
     pairs = sorted({(rng.randrange(64), rng.randrange(8)) for _ in range(8)})
     check_sampled(cuda_lib, case, y, pairs, "fp8 mixed batch")
+
+
+# ------------------------------------------------------------------ several query rows
+def rows_case(R, *args, **kw):
+    """A case whose q holds R query rows per sequence: [B, R, Hq, D]."""
+    case = pi.make_case(*args, **kw)
+    g = torch.Generator().manual_seed(1000 + R)
+    B, Hq, D = case.q.shape
+    case.q = torch.randn((B, R, Hq, D), generator=g).to(case.q.dtype).to(case.q.device)
+    return case
+
+
+@pytest.mark.parametrize("R,hq,hkv", [(2, 8, 8), (4, 16, 8), (4, 32, 8), (2, 64, 8),
+                                      (8, 32, 8), (3, 24, 8)])
+def test_query_rows(cuda_lib, R, hq, hkv):
+    lens = [1, 3, 17, 1025, 4097]       # includes contexts shorter than R
+    case = rows_case(R, 5, hq, hkv, 128, 16, lens, seed=90 + R, poison="kv_nan")
+    y = run(cuda_lib, case)
+    assert y.shape == case.q.shape
+    assert_parity(to_np(y), oracle_rows_case(case), what=f"rows R={R} {hq}/{hkv}")
+    no_device_errors(cuda_lib)
+
+
+@pytest.mark.parametrize("S", [1, 3, 9])
+def test_query_rows_splits_with_empty_columns(cuda_lib, S):
+    # L = 33, 16-token splits: the last split holds tokens 32.. only, which row 0
+    # (limit L - R + 1 = 30) cannot see
+    case = rows_case(4, 2, 16, 8, 128, 16, [33, 100], seed=95).to("cuda")
+    y = run(cuda_lib, case, splits=S)
+    assert_parity(to_np(y), oracle_rows_case(case), what=f"rows splits={S}")
+
+
+def test_query_rows_hybrid_and_fp8(cuda_lib):
+    case = rows_case(2, 1, 24, 4, 256, 784, [5000], seed=96)
+    assert_parity(to_np(run(cuda_lib, case)), oracle_rows_case(case), what="rows hybrid")
+    case = rows_case(4, 3, 32, 8, 128, 16, [700, 4097, 9], seed=97, kv_dtype="fp8")
+    assert_parity(to_np(run(cuda_lib, case)), oracle_rows_case(case), what="rows fp8")
+
+
+def test_one_row_equals_single_query(cuda_lib):
+    case = pi.make_case(3, 32, 8, 128, 16, [2000, 5, 3333], seed=98).to("cuda")
+    a = run(cuda_lib, case)
+    q4 = case.q.unsqueeze(1).contiguous()
+    b = cuda_lib.decode(q4, case.k_cache, case.v_cache, case.block_tables, case.seq_lens,
+                        case.scale, max_seq_len=case.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b[:, 0])
 
 
 # ------------------------------------------------------------------ device-side errors
