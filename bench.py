@@ -19,7 +19,7 @@ rotating over enough independent copies of the cell (>= 512 MiB of KV in total,
 four times the L2) that every call reads HBM, as an engine replays its layers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload grid|hybrid|mixed|first|cell|window]
+                    [--workload grid|hybrid|mixed|first|cell|window|rows]
                     [--cell Hq,Hkv,B,L,D,bs]
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
@@ -61,7 +61,7 @@ class Inst:
     """One set of device inputs for a decode call."""
 
     def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, exact,
-                 window=0, fp8=False):
+                 window=0, fp8=False, rows=1):
         gen = torch.Generator(device=device)
         gen.manual_seed(seed)
         dt = torch.bfloat16
@@ -74,7 +74,8 @@ class Inst:
         back = [min(n, -(-window // bs) + 1) if (window > 0 and not exact) else n for n in nblk]
         nb = max(1, int(math.ceil(sum(back) * pool_factor)))
         self.num_blocks = nb
-        self.q = torch.randn((B, Hq, D), generator=gen, device=device).to(dt)
+        qshape = (B, rows, Hq, D) if rows > 1 else (B, Hq, D)
+        self.q = torch.randn(qshape, generator=gen, device=device).to(dt)
         if exact:
             # live tokens N(0,1); spare blocks and unwritten tails keep the fill
             fill = float("nan") if poison == "nan" else 0.0
@@ -109,8 +110,9 @@ class Cell:
     """A decode configuration: inputs for the step, plus copies for the curve."""
 
     def __init__(self, B, Hq, Hkv, D, bs, lens, seed, device, poison=None, pool_factor=2.0,
-                 tag="", window=0, fp8=None):
+                 tag="", window=0, fp8=None, rows=1):
         self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
+        self.rows = rows
         self.window = window
         self.fp8 = KV_FP8 if fp8 is None else fp8
         self.kv_elem = 1 if self.fp8 else 2
@@ -118,7 +120,7 @@ class Cell:
         self.tag = tag
         self.seed, self.device, self.poison, self.pool_factor = seed, device, poison, pool_factor
         self.insts = [Inst(B, Hq, Hkv, D, bs, lens, seed, device, poison, pool_factor, True,
-                           window, self.fp8)]
+                           window, self.fp8, rows)]
         self.max_len = max(lens)
         self.scale = float(np.float32(1.0 / math.sqrt(D)))
         self.ws = None
@@ -127,7 +129,7 @@ class Cell:
         for i in range(len(self.insts), n):
             self.insts.append(Inst(self.B, self.Hq, self.Hkv, self.D, self.bs, self.lens,
                                    self.seed + 7919 * i, self.device, self.poison,
-                                   self.pool_factor, False, self.window, self.fp8))
+                                   self.pool_factor, False, self.window, self.fp8, self.rows))
 
     def read_lens(self):
         """Tokens each sequence's query attends to (the window bounds them)."""
@@ -139,7 +141,7 @@ class Cell:
     def alg_bytes(self) -> int:
         """Bytes the method must move: KV, the live block-table entries, q, out, seq_lens."""
         table = sum(-(-L // self.bs) + 1 for L in self.read_lens()) * 4
-        return self.kv_bytes() + table + 2 * self.B * self.Hq * self.D * 2 + 4 * self.B
+        return self.kv_bytes() + table + 2 * self.B * self.rows * self.Hq * self.D * 2 + 4 * self.B
 
     def call(self, pa, stream=None, i=0):
         x = self.insts[i]
@@ -197,6 +199,18 @@ def build_workload(name, device, seed=0, cell_spec=None):
                 "block_size": 16, "window": 1024, "seq_lens": GRID_LENS,
                 "batches": GRID_BATCHES, "cells": len(cells),
                 "bytes": "KV of the window only: min(L, 1024) tokens per sequence"}
+    elif name == "rows":
+        # speculative decode: 4 query rows per sequence, 32 query / 8 KV heads, head 128
+        i = 0
+        for B in GRID_BATCHES:
+            for L in GRID_LENS:
+                cells.append(Cell(B, 32, 8, 128, 16, [L] * B, seed + i, device,
+                                  tag=f"rows4 32/8 B={B} L={L}", rows=4))
+                i += 1
+        desc = {"workload": "speculative_decode_rows", "Hq": 32, "Hkv": 8, "head_dim": 128,
+                "block_size": 16, "query_rows": 4, "seq_lens": GRID_LENS,
+                "batches": GRID_BATCHES, "cells": len(cells),
+                "bytes": "KV read once per (sequence, KV head) for all 4 rows"}
     elif name == "first":
         cells.append(Cell(1, 8, 8, 128, 16, [512], seed, device, tag="first"))
         desc = {"workload": "first_config", "batch": 1, "Hq": 8, "Hkv": 8, "head_dim": 128,
@@ -569,7 +583,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="grid",
-                    choices=["grid", "hybrid", "mixed", "first", "cell", "window"])
+                    choices=["grid", "hybrid", "mixed", "first", "cell", "window", "rows"])
     ap.add_argument("--cell", default=None, help="Hq,Hkv,B,L,D,block_size for --workload cell")
     ap.add_argument("--no-curve", action="store_true", help="skip the steady-state curve")
     ap.add_argument("--seed", type=int, default=0)
