@@ -72,7 +72,7 @@ struct Cfg {
   static constexpr int SMEM = RING + NW * STAGE_BYTES + FIXED;
   static_assert((TW * CPR) % 32 == 0, "tile shape");
   static_assert(DEPTH >= 2, "need at least two slots per warp");
-  static_assert(NW * GT * (D + 2) * 4 <= RING + NW * STAGE_BYTES, "CTA merge must fit");
+  static_assert(NW * GT * (D + 6) * 4 <= RING + NW * STAGE_BYTES, "CTA merge must fit");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
@@ -404,53 +404,85 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) l[nt][h] += __shfl_xor_sync(0xffffffffu, l[nt][h], o2);
 
-  // ---- merge the warps (the ring is free: every copy has landed and been consumed)
+  // ---- merge the warps (the ring is free: every copy has landed and been consumed).
+  // Each warp first rescales its state to the CTA-wide maximum of every column, so
+  // that the final pass only sums: it reads 8 consecutive d of one column per item
+  // as two 16-byte words per warp and writes them with one 16-byte store.
+  // Accumulator rows are padded by 4 floats, so that the fragment writes (columns
+  // 2 tig + {0, 1}, rows gid) fall in distinct banks.
+  constexpr int AP = D + 4;
   __syncthreads();
-  float* mw = reinterpret_cast<float*>(ring);  // [NW][GT]
-  float* lw = mw + kWarps * GT;                // [NW][GT]
-  float* aw = lw + kWarps * GT;                // [NW][GT][D]
+  float* mw = reinterpret_cast<float*>(ring);  // [NW][GT] running maxima
+  float* lw = mw + kWarps * GT;                // [NW][GT] rescaled denominators
+  float* aw = lw + kWarps * GT;                // [NW][GT][AP] rescaled accumulators
+  if (gid == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mw[warp * GT + nt * 8 + 2 * tig] = m[nt][0];
+      mw[warp * GT + nt * 8 + 2 * tig + 1] = m[nt][1];
+    }
+  }
+  __syncthreads();
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int g0 = nt * 8 + 2 * tig;
-    if (gid == 0) {
-      mw[warp * GT + g0] = m[nt][0];
-      mw[warp * GT + g0 + 1] = m[nt][1];
-      lw[warp * GT + g0] = l[nt][0];
-      lw[warp * GT + g0 + 1] = l[nt][1];
+    const int c0 = nt * 8 + 2 * tig;
+    float f[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GT + c0 + h]);
+      // a warp that saw no token of the column (m = -inf) contributes nothing
+      f[h] = m[nt][h] == -INFINITY ? 0.f : exp2f(m[nt][h] - M);
     }
+    if (gid == 0) {
+      lw[warp * GT + c0] = l[nt][0] * f[0];
+      lw[warp * GT + c0 + 1] = l[nt][1] * f[1];
+    }
+    float* a0 = aw + (warp * GT + c0) * AP;
 #pragma unroll
     for (int dd = 0; dd < C::KS; ++dd) {
       const int d0 = dd * 16 + gid;
-      aw[(warp * GT + g0) * D + d0] = o[nt][dd][0];
-      aw[(warp * GT + g0 + 1) * D + d0] = o[nt][dd][1];
-      aw[(warp * GT + g0) * D + d0 + 8] = o[nt][dd][2];
-      aw[(warp * GT + g0 + 1) * D + d0 + 8] = o[nt][dd][3];
+      a0[d0] = o[nt][dd][0] * f[0];
+      a0[AP + d0] = o[nt][dd][1] * f[1];
+      a0[d0 + 8] = o[nt][dd][2] * f[0];
+      a0[AP + d0 + 8] = o[nt][dd][3] * f[1];
     }
   }
   __syncthreads();
 
   const bool single = n_splits == 1;
   const size_t pidx = ((size_t)b * p.Hkv + kvh) * p.S + split;
-  for (int i = threadIdx.x; i < cols * D; i += kThreads) {
-    const int g = i / D, d = i - (i / D) * D;  // g: column
-    float M = -INFINITY;
+  constexpr int DV = D / 8;  // items per column
+  for (int it = threadIdx.x; it < cols * DV; it += kThreads) {
+    const int g = it / DV, d0 = (it % DV) * 8;  // g: column
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float den = 0.f, M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GT + g]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {  // a column whose row sees no token of this split stays empty
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float e = exp2f(mw[w * GT + g] - M);  // idle warps: m = -inf, weight 0
-        num += e * aw[(w * GT + g) * D + d];
-        den += e * lw[w * GT + g];
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float4* src = reinterpret_cast<const float4*>(aw + (w * GT + g) * AP + d0);
+      const float4 x = src[0], y = src[1];
+      v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+      den += lw[w * GT + g];
+      M = fmaxf(M, mw[w * GT + g]);
     }
-    num *= p.v_scale;  // cache values are stored values times v_scale (1 unless fp8)
+    // cache values are stored values times v_scale (1 unless fp8); a column whose
+    // row sees no token of this split has M = -inf and den = 0
     if (single) {
-      out[qrow(g) * D + d] = from_f32<T>(den > 0.f ? num / den : 0.f);
+      const float r = den > 0.f ? p.v_scale / den : 0.f;
+      uint4 pk;
+      pk.x = pack2<T>(v[0] * r, v[1] * r);
+      pk.y = pack2<T>(v[2] * r, v[3] * r);
+      pk.z = pack2<T>(v[4] * r, v[5] * r);
+      pk.w = pack2<T>(v[6] * r, v[7] * r);
+      *reinterpret_cast<uint4*>(out + qrow(g) * D + d0) = pk;
     } else {
-      p.ws_acc[(pidx * cols + g) * D + d] = num;
-      if (d == 0) {
+      const float vs = p.v_scale;
+      float4* dst = reinterpret_cast<float4*>(p.ws_acc + (pidx * cols + g) * D + d0);
+      dst[0] = make_float4(v[0] * vs, v[1] * vs, v[2] * vs, v[3] * vs);
+      dst[1] = make_float4(v[4] * vs, v[5] * vs, v[6] * vs, v[7] * vs);
+      if (d0 == 0) {
         p.ws_m[pidx * cols + g] = M;
         p.ws_l[pidx * cols + g] = den;
       }
@@ -463,13 +495,14 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 // (the flash-decoding reduction). Splits where a row sees no token carry m = -inf
 // and weight 0. M is finite whenever the row sees a token; a row that sees none
 // (several query rows, short context) is written as zeros. 256 threads: 64 output
-// elements x 4 split lanes.
+// elements x 4 split lanes. Every warp reduces the maxima and sums itself with
+// shuffles (lane s % 32 holds split s), so one barrier remains: the sum over the
+// four split lanes.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   pdl_wait();  // the partials of the decode grid are complete and visible
   pdl_launch_dependents();
-  __shared__ float ms[kMaxSplits], ws[kMaxSplits];
-  __shared__ float red[8], part[4][64];
+  __shared__ float part[4][64];
   const int b = blockIdx.z, row = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
   const int G = p.G, kvh = h / G, g = h - kvh * G;
   const int cols = G * p.q_len, c = row * G + g;  // the partials' column of (row, head)
@@ -480,56 +513,52 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   const int n = (L + p.P - 1) / p.P;
   if (n <= 1) return;  // written by the decode grid
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int dl = tid & 63, sl = tid >> 6;
   const int d = blockIdx.x * 64 + dl;
   const float* acc = p.ws_acc + (base * cols + c) * D + d;
+  const float* pm = p.ws_m + base * cols + c;
+  const float* pl = p.ws_l + base * cols + c;
 
-  // The accumulators do not depend on the weights: request the first 16 splits of
-  // this thread's lane together with the maxima and sums (one round trip).
-  constexpr int kPre = 16;
+  // One round trip: this thread's accumulators of splits sl + 4 i (i < 16) and the
+  // warp's maxima and sums of splits lane and lane + 32.
+  constexpr int kPre = 16, kReg = 2;  // 4 * kPre == 32 * kReg
   float av[kPre];
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
     const int s2 = sl + 4 * i;
     av[i] = s2 < n ? __ldcg(acc + (size_t)s2 * cols * D) : 0.f;
   }
-
-  float mx = -INFINITY;
-  for (int s2 = tid; s2 < n; s2 += 256) {
-    const float v = __ldcg(p.ws_m + (base + s2) * cols + c);
-    ms[s2] = v;
-    ws[s2] = __ldcg(p.ws_l + (base + s2) * cols + c);
-    mx = fmaxf(mx, v);
-  }
-  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  float M = red[0];
+  float mr[kReg], lr[kReg];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float den = 0.f;
-  for (int s2 = tid; s2 < n; s2 += 256) {
-    const float w = M == -INFINITY ? 0.f : exp2f(ms[s2] - M);
-    den += w * ws[s2];
-    ms[s2] = w;  // ms now holds the weights
+  for (int j = 0; j < kReg; ++j) {
+    const int s2 = lane + 32 * j;
+    mr[j] = s2 < n ? __ldcg(pm + (size_t)s2 * cols) : -INFINITY;
+    lr[j] = s2 < n ? __ldcg(pl + (size_t)s2 * cols) : 0.f;
   }
+  float M = fmaxf(mr[0], mr[1]);
+  for (int s2 = lane + 32 * kReg; s2 < n; s2 += 32) M = fmaxf(M, __ldcg(pm + (size_t)s2 * cols));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float wr[kReg], den = 0.f;
+#pragma unroll
+  for (int j = 0; j < kReg; ++j) {
+    wr[j] = M == -INFINITY ? 0.f : exp2f(mr[j] - M);
+    den += wr[j] * lr[j];
+  }
+  for (int s2 = lane + 32 * kReg; s2 < n; s2 += 32)
+    den += M == -INFINITY ? 0.f : exp2f(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(pl + (size_t)s2 * cols);
+#pragma unroll
   for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane == 0) red[warp] = den;
-  __syncthreads();
-  den = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) den += red[w];
 
   float num = 0.f;
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
-    const int s2 = sl + 4 * i;
-    if (s2 < n) num += ms[s2] * av[i];
+    const int s2 = sl + 4 * i;  // held by lane s2 % 32 in wr[s2 / 32] (s2 / 32 == i / 8)
+    num += __shfl_sync(0xffffffffu, wr[i / 8], s2 & 31) * av[i];
   }
-#pragma unroll 8
-  for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4) num += ms[s2] * __ldcg(acc + (size_t)s2 * cols * D);
+  for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4)
+    num += M == -INFINITY ? 0.f : exp2f(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(acc + (size_t)s2 * cols * D);
   part[sl][dl] = num;
   __syncthreads();
   if (sl == 0) {

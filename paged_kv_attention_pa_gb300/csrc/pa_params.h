@@ -8,7 +8,8 @@
 
 namespace pa {
 
-// Split counts are bounded by the merge kernel's shared weights.
+// Split counts are bounded, so that the partials stay a small fraction of the KV
+// bytes at any context length.
 constexpr int kMaxSplits = 1024;
 constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost dominates
 constexpr int kTokenQuantum = 16;   // partition sizes are multiples of the warp tile
