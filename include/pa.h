@@ -101,6 +101,12 @@ typedef void* pa_stream_t; /* cudaStream_t */
  *           token gets zeros. Every K/V tile is read once for all rows and heads of
  *           its KV head. Limits: G * R <= 32 at head_dim 128, <= 16 at 256; not
  *           combined with a window (PA_ERR_UNSUPPORTED).
+ *   flags   0 or PA_FLAG_DETERMINISTIC. By default, when a long context is split
+ *           across CTAs, the splits share out its last eighth tile by tile as
+ *           they finish their own shares, so the order of the fp32 sums depends
+ *           on timing and repeated calls may differ in the last bit (each within
+ *           the usual error). PA_FLAG_DETERMINISTIC keeps fixed splits: repeated
+ *           calls give bitwise identical outputs. Other bits: PA_ERR_INVALID_ARG.
  * All other fields mean what the pa_decode parameters of the same name mean.
  */
 typedef struct pa_decode_args {
@@ -119,17 +125,23 @@ typedef struct pa_decode_args {
   int32_t kv_dtype; /* pa_kv_dtype */
   float k_scale, v_scale;
   int32_t q_len;
+  uint32_t flags;
 } pa_decode_args;
+
+#define PA_FLAG_DETERMINISTIC 1u
 
 /*
  * Workspace bytes pa_decode needs for these sizes on the current device. The
- * workspace holds the device error word (first 4 bytes, which must be zero
- * before the first call: pa_workspace_init or any memset) and the fp32 split
- * partials (m, l, acc), which every call writes before it reads them. One
- * workspace serves calls of any shape that fit its size; calls that overlap on
- * the GPU must not share one. Returns 0 for invalid sizes (max_seq_len must be
- * > 0 here).
+ * workspace starts with a header of PA_WORKSPACE_HEADER_BYTES that must be zero
+ * before the first call (pa_workspace_init or any memset): the device error word
+ * (first 4 bytes) and one counter per (sequence, KV head) through which the
+ * splits of a sequence share out the tail of its context; every call leaves the
+ * counters zero again. After the header come the fp32 split partials (m, l, acc),
+ * which every call writes before it reads them. One workspace serves calls of
+ * any shape that fit its size; calls that overlap on the GPU must not share one.
+ * Returns 0 for invalid sizes (max_seq_len must be > 0 here).
  */
+#define PA_WORKSPACE_HEADER_BYTES 8448u
 size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size, int max_seq_len);
 
 /* Same, for pa_decode_ex's argument set (pointer fields are ignored). */
@@ -154,7 +166,7 @@ size_t pa_decode_ex_workspace_bytes(const pa_decode_args* args);
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D))
  *   dtype         PA_F16 or PA_BF16 for q, caches and out
  *   workspace     device scratch of >= pa_decode_workspace_bytes(...) bytes,
- *                 256-byte aligned, its first 4 bytes zero before first use
+ *                 256-byte aligned, its header zero before first use
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE,
  * PA_ERR_OUT_OF_RANGE (max_seq_len above capacity), PA_ERR_CUDA.
  */
@@ -207,7 +219,7 @@ pa_status pa_set_device(int device);
  *    its header (a synchronous cudaMemset); make that first call before any
  *    stream capture on that device.
  *  - Every call on a device shares the one array, which keeps the last call's
- *    contents. Nothing in it needs to start at zero except the error word,
+ *    contents. Nothing in it needs to start at zero except its header,
  *    cleared at that first call. Calls that may overlap on the GPU (different
  *    streams, concurrent threads) race on it: serialise them.
  *  - Device-side range errors (PA_DEVERR_*) are recorded in the array's header

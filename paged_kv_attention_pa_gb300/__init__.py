@@ -29,6 +29,8 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, \
 PA_F16, PA_BF16 = 0, 1
 PA_KV_AS_DTYPE, PA_KV_FP8_E4M3 = 0, 1
 PA_DEVERR_BLOCK_INDEX, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT = 1, 2, 4
+PA_FLAG_DETERMINISTIC = 1
+PA_WORKSPACE_HEADER_BYTES = 8448
 MAX_GQA_GROUP = 16
 
 # Every symbol include/pa.h declares, with its ctypes signature.
@@ -61,6 +63,7 @@ class DecodeArgs(ctypes.Structure):
         ("scale", _c.c_float), ("dtype", _c.c_int32), ("splits", _c.c_int32),
         ("window", _c.c_int32), ("kv_dtype", _c.c_int32),
         ("k_scale", _c.c_float), ("v_scale", _c.c_float), ("q_len", _c.c_int32),
+        ("flags", _c.c_uint32),
     ]
 
 
@@ -120,7 +123,8 @@ def _stream_handle(device: torch.device, stream) -> int:
 
 def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
               max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0,
-              k_scale: float = 1.0, v_scale: float = 1.0) -> DecodeArgs:
+              k_scale: float = 1.0, v_scale: float = 1.0,
+              deterministic: bool = False) -> DecodeArgs:
     """Check shapes / dtypes / devices and fill a pa_decode_args. q is [B, Hq, D], or
     [B, R, Hq, D] for R causal query rows per sequence."""
     if q.dim() not in (3, 4) or k_cache.dim() != 4 or v_cache.dim() != 4:
@@ -166,6 +170,7 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     a.q_len = R
     a.kv_dtype = PA_KV_FP8_E4M3 if fp8 else PA_KV_AS_DTYPE
     a.k_scale, a.v_scale = (float(k_scale), float(v_scale)) if fp8 else (1.0, 1.0)
+    a.flags = PA_FLAG_DETERMINISTIC if deterministic else 0
     return a
 
 
@@ -190,7 +195,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
            out: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
            splits: int = 0, workspace: Optional[torch.Tensor] = None, stream=None,
-           window: int = 0, k_scale: float = 1.0, v_scale: float = 1.0) -> torch.Tensor:
+           window: int = 0, k_scale: float = 1.0, v_scale: float = 1.0,
+           deterministic: bool = False) -> torch.Tensor:
     """out[b, h] = softmax(scale * q[b,h] . K_b^T) V_b over the paged context of sequence b.
 
     q [B, Hq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D]; block_tables
@@ -198,13 +204,16 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     bounds seq_lens (pass it: it sets the split plan; None means the table's
     capacity). splits > 0 forces at most that many context splits. window > 0
     attends to the last `window` tokens only. float8_e4m3fn caches are read as
-    stored value * k_scale / v_scale. Asynchronous on the current (or given) stream.
+    stored value * k_scale / v_scale. deterministic=True keeps fixed context splits, so
+    that repeated calls are bitwise identical (by default the splits of a long context
+    share out its tail as they finish, and the last bit may vary from call to call).
+    Asynchronous on the current (or given) stream.
     """
     lib = load()
     if out is None:
         out = torch.empty_like(q)
     args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, splits,
-                     window, k_scale, v_scale)
+                     window, k_scale, v_scale, deterministic)
     _ensure_device(lib, q.device.index)
     sh = _stream_handle(q.device, stream)
     ws = workspace if workspace is not None else workspace_for(args, q.device, sh)

@@ -75,8 +75,9 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
 }
 
 // ---------------------------------------------------------------- workspace
-// [0, 256)   device error word (uint32) + padding
-// m, l       B*Hkv*S*G fp32 each        (only when S > 1)
+// [0, 256)            device error word (uint32) + padding
+// [256, kHeaderBytes)  shared-tile counters, one int per (sequence, KV head)
+// m, l                 B*Hkv*S*G fp32 each        (only when S > 1)
 // acc        B*Hkv*S*G*D fp32           (only when S > 1)
 struct WsLayout {
   size_t m, l, acc, total;
@@ -84,7 +85,7 @@ struct WsLayout {
 
 WsLayout ws_layout(int64_t B, int64_t Hkv, int64_t G, int64_t D, int64_t S) {
   WsLayout w{};
-  size_t off = 256;
+  size_t off = pa::kHeaderBytes;
   if (S > 1) {
     const size_t parts = (size_t)(B * Hkv * S * G);
     w.m = off;
@@ -134,6 +135,7 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
     if ((int64_t)a->Hq * rows > 65535) return PA_ERR_INVALID_ARG;     // merge grid limit
   }
   if (a->kv_dtype != PA_KV_AS_DTYPE && a->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (a->flags & ~PA_FLAG_DETERMINISTIC) return PA_ERR_INVALID_ARG;
   if (a->kv_dtype == PA_KV_FP8_E4M3 &&
       !(a->k_scale > 0.f && a->v_scale > 0.f && a->k_scale < INFINITY && a->v_scale < INFINITY))
     return PA_ERR_INVALID_ARG;
@@ -289,6 +291,15 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.max_seq_len = (int)max_len;
   p.S = plan.S;
   p.P = plan.P;
+  // static share per split; the rest of each context is claimed tile by tile
+  p.Ps = plan.P;
+  const long long split_bytes = (long long)plan.P * 2 * a->D * (a->kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2);
+  if (plan.S > 1 && !(a->flags & PA_FLAG_DETERMINISTIC) && pa::kStealDiv > 0 &&
+      split_bytes >= pa::kStealMinBytes && (int64_t)a->B * a->Hkv <= pa::kStealUnits) {
+    const int shared = (plan.P / pa::kStealDiv) / pa::kTokenQuantum * pa::kTokenQuantum;
+    p.Ps = plan.P - shared;
+  }
+  p.steal = reinterpret_cast<int*>(ws + 256);
   p.window = a->window;
   p.q_len = rows;
   p.kv_fp8 = a->kv_dtype == PA_KV_FP8_E4M3;

@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 
   // ---- prologue: everything the first copies depend on is requested at once (one
   // round trip): the context length, the query fragments and, speculatively, the
-  // block-table entries of this warp's first tiles. Entries are read only inside
-  // the table row; those past the sequence are ignored, never dereferenced.
+  // block-table entries of this warp's first static tiles. Entries are read only
+  // inside the table row; those past the sequence are ignored, never dereferenced.
   const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks;
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
   int L = __ldg(p.seq_lens + b);
@@ -141,16 +141,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     validate_len();
     t_lo = max(0, L - p.window);
   }
-  const int t_begin = t_lo + split * p.P;
-  // block-table entry of token t0(k) + lane, for this warp's k-th tile
-  auto table_entry = [&](int k) -> int {
-    const long long t = (long long)t_begin + (long long)(warp + k * kWarps) * C::TW + lane;
-    if (lane >= C::TW || t >= cap) return 0;
+  // This split owns Ps tokens from s_lo (its static share; Ps == P unless the
+  // remaining tokens of the sequence are shared out tile by tile, see below).
+  const int s_lo = t_lo + split * p.Ps;
+  auto static_t0 = [&](int k) { return s_lo + (warp + k * kWarps) * C::TW; };
+  // lanes 0..TW-1: block-table entry of token t0 + lane (0 where there is none)
+  auto entry_of = [&](int t0) -> int {
+    const long long t = (long long)t0 + lane;
+    if (lane >= C::TW || t0 < 0 || t >= cap) return 0;
     return __ldg(bt_row + (int)t / p.block_size);
   };
   int pe[C::DEPTH];  // entries of tiles 0 .. DEPTH-1
 #pragma unroll
-  for (int k = 0; k < C::DEPTH; ++k) pe[k] = table_entry(k);
+  for (int k = 0; k < C::DEPTH; ++k) pe[k] = entry_of(static_t0(k));
   // query fragments (B operand of the score MMA), unscaled, zero for padded heads
   uint32_t qf[NT][C::KS][2];
   {
@@ -186,17 +189,26 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         out[qrow(i / D) * D + i % D] = from_f32<T>(0.f);
     return;
   }
-  if (t_begin >= L) return;  // this split lies past the sequence: nothing to do
-  const int t_end = min(L, t_begin + p.P);
-  const int n_tiles = (t_end - t_begin + C::TW - 1) / C::TW;
+  if (t_lo + split * p.P >= L) return;  // this split lies past the sequence: nothing to do
   const int n_splits = (L - t_lo + p.P - 1) / p.P;
+  // Work sharing among the splits of one (sequence, KV head). Every split streams
+  // its static share; the tokens past the n static shares go out one 16-token tile
+  // at a time from a counter in the workspace, so that splits on faster SMs take
+  // more of them and all end together. The merge kernel resets the counter.
+  const bool steal = p.Ps < p.P && n_splits > 1;
+  const int s_hi = steal ? min(L, s_lo + p.Ps) : min(L, t_lo + (split + 1) * p.P);
+  const int n_stat = (s_hi - s_lo + C::TW - 1) / C::TW;  // static tiles of the CTA (>= 1)
+  const int ns = warp < n_stat ? (n_stat - warp + kWarps - 1) / kWarps : 0;  // this warp's
+  const int dyn_lo = steal ? min(L, t_lo + n_splits * p.Ps) : L;
+  const int n_dyn = (L - dyn_lo + C::TW - 1) / C::TW;  // shared tiles of the sequence
+  int* const ctr = steal ? p.steal + (size_t)b * p.Hkv + kvh : nullptr;
   // Causal limit of each of this thread's columns: row i sees tokens t < L - R + i + 1
-  // (all of them when R = 1), and this split only its own tokens t < t_end.
+  // (all of them when R = 1).
   int lim[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) lim[nt][h] = min(t_end, L - R + (nt * 8 + 2 * tig + h) / G + 1);
+    for (int h = 0; h < 2; ++h) lim[nt][h] = L - R + (nt * 8 + 2 * tig + h) / G + 1;
 
   // ---- per-warp copy pipeline
   const uint64_t pol = l2_evict_first_policy();
@@ -205,15 +217,12 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       reinterpret_cast<const uint8_t*>(p.v_cache) - reinterpret_cast<const uint8_t*>(p.k_cache);
   uint8_t* my_ring = ring + warp * C::DEPTH * C::SLOT_BYTES;
   const uint32_t my_ring_s = smem_addr(my_ring);
-  const int my_tiles = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
 
-  // Issue the copies of this warp's k-th tile (a commit group even when empty);
-  // phys is this lane's block-table entry for the tile, validated here.
-  auto issue = [&](int k, int phys) {
-    if (k < my_tiles) {
-      const int j = warp + k * kWarps;
-      const int t0 = t_begin + j * C::TW;
-      const int nv = min(C::TW, t_end - t0);
+  // Issue the copies of this warp's k-th tile, tokens t0 .. (a commit group even
+  // when t0 < 0: no tile); phys is this lane's block-table entry, validated here.
+  auto issue = [&](int k, int phys, int t0) {
+    if (t0 >= 0) {
+      const int nv = min(C::TW, L - t0);
       // lanes 0..TW-1 resolve one row each: cache row index of token t0 + lane
       uint32_t ridx = 0;
       if (lane < nv) {
@@ -243,8 +252,69 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     cp_async_commit();
   };
 
+  // This warp's tiles: its static ones, then shared ones. A shared tile is claimed
+  // one step before its block-table entry is requested (lane 0's atomic, still in
+  // flight meanwhile). The stream ends at the first claim past the shared tiles,
+  // so no claim is left unconsumed.
+  int kk_next = 0;        // index of the next tile to define
+  int claim = 0;          // lane 0: result of the claim in flight
+  bool claiming = false;  // a claim is in flight
+  bool more = n_dyn > 0;  // shared tiles may remain
+  auto next_t0 = [&]() -> int {  // t0 of the next tile of the stream, -1 past its end
+    const int kk = kk_next++;
+    int t0 = -1;
+    if (kk < ns) {
+      t0 = static_t0(kk);
+    } else if (more) {
+      if (!claiming && lane == 0) claim = atomicAdd(ctr, 1);
+      const int g = __shfl_sync(0xffffffffu, claim, 0);
+      claiming = false;
+      if (g < n_dyn)
+        t0 = dyn_lo + g * C::TW;
+      else
+        more = false;
+    }
+    if (more && !claiming && kk + 1 >= ns) {  // claim the tile after this one now
+      if (lane == 0) claim = atomicAdd(ctr, 1);
+      claiming = true;
+    }
+    return t0;
+  };
+  // The first DEPTH tiles: the static ones among the first DEPTH - 1 go out at
+  // once; the shared ones are claimed together (one atomic) and go out when their
+  // entries arrive; then the claim of tile DEPTH goes out.
 #pragma unroll
-  for (int k = 0; k < C::DEPTH - 1; ++k) issue(k, pe[k]);
+  for (int k = 0; k < C::DEPTH - 1; ++k)
+    if (k < ns) issue(k, pe[k], static_t0(k));
+  int tq[C::DEPTH];  // t0 of tiles k .. k + DEPTH - 1
+  {
+    const int m0 = ns < C::DEPTH ? C::DEPTH - ns : 0;
+    int g0 = 0;
+    if (m0 > 0 && more) {
+      if (lane == 0) g0 = atomicAdd(ctr, m0);
+      g0 = __shfl_sync(0xffffffffu, g0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < C::DEPTH; ++k) {
+      if (k < ns) {
+        tq[k] = static_t0(k);
+      } else {
+        const int g = g0 + (k - ns);
+        if (more && g >= n_dyn) more = false;
+        tq[k] = more ? dyn_lo + g * C::TW : -1;
+        pe[k] = entry_of(tq[k]);  // not a static tile: look its entry up now
+      }
+    }
+    kk_next = C::DEPTH;
+    if (more && ns <= C::DEPTH) {
+      if (lane == 0) claim = atomicAdd(ctr, 1);
+      claiming = true;
+    }
+  }
+
+#pragma unroll
+  for (int k = 0; k < C::DEPTH - 1; ++k)
+    if (k >= ns) issue(k, pe[k], tq[k]);
   int next_entry = pe[C::DEPTH - 1];  // for the tile issued in the first loop iteration
 
   // running state: this thread's heads are nt*8 + 2*tig + {0, 1}
@@ -263,13 +333,17 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   uint8_t* my_stage = ring + C::RING + warp * C::STAGE_BYTES;  // fp8 only
   const float sl2 = p.scale_log2;
 
-  for (int k = 0; k < my_tiles; ++k) {
+  for (int k = 0; tq[0] >= 0; ++k) {  // tile k of the stream: tokens tq[0] ..
     const int entry = next_entry;
-    next_entry = table_entry(k + C::DEPTH);  // one iteration ahead of its use
-    issue(k + C::DEPTH - 1, entry);
+    const int t_new = next_t0();    // tile k + DEPTH
+    next_entry = entry_of(t_new);   // one iteration ahead of its use
+    issue(k + C::DEPTH - 1, entry, tq[C::DEPTH - 1]);
     cp_async_wait<C::DEPTH - 1>();  // tile k has landed (for this lane's copies)
-    const int j = warp + k * kWarps;
-    const int nv = min(C::TW, t_end - (t_begin + j * C::TW));
+    const int t0 = tq[0];
+#pragma unroll
+    for (int i = 0; i + 1 < C::DEPTH; ++i) tq[i] = tq[i + 1];
+    tq[C::DEPTH - 1] = t_new;
+    const int nv = min(C::TW, L - t0);
     uint32_t kt, vt;
     if constexpr (F8) {
       // widen this tile's V bytes to fp16 in the warp's staging tile (the PV MMA reads
@@ -347,8 +421,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 #pragma unroll
       for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
     // tokens gid and gid + 8 of the tile; -inf by select past each column's limit
-    // (seq_len, this split's end, and the causal limit of the column's query row)
-    const int tok0 = t_begin + j * C::TW + gid, tok1 = tok0 + 8;
+    // (seq_len, and the causal limit of the column's query row); rows past seq_len
+    // were never loaded
+    const int tok0 = t0 + gid, tok1 = tok0 + 8;
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -512,6 +587,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   if (p.window > 0) L = min(L, p.window);  // tokens the splits cover
   const int n = (L + p.P - 1) / p.P;
   if (n <= 1) return;  // written by the decode grid
+  // the decode grid is done with this (sequence, KV head)'s tile counter: rearm it
+  if (p.Ps < p.P && blockIdx.x == 0 && row == 0 && g == 0 && threadIdx.x == 0)
+    p.steal[(size_t)b * p.Hkv + kvh] = 0;
   const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
   const int tid = threadIdx.x, lane = tid & 31;
   const int dl = tid & 63, sl = tid >> 6;

@@ -25,7 +25,7 @@ void* g_scratch_addr[kMaxDevices] = {};  // device address of the array, per dev
 
 // Once per device, with that device current: look up the array's device address
 // (the host-side name is only a stand-in, never a device pointer) and zero the
-// 256-byte header that holds the device error word.
+// workspace header (the device error word and the shared-tile counters).
 pa_status scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -40,7 +40,7 @@ pa_status scratch_for_current_device(void** out) {
       cudaGetLastError();
       return PA_ERR_CUDA;
     }
-    if (cudaMemset(addr, 0, 256) != cudaSuccess) {
+    if (cudaMemset(addr, 0, PA_WORKSPACE_HEADER_BYTES) != cudaSuccess) {
       cudaGetLastError();
       return PA_ERR_CUDA;
     }

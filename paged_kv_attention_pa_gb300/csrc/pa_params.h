@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include "pa.h"
+
 namespace pa {
 
 // Split counts are bounded, so that the partials stay a small fraction of the KV
@@ -16,6 +18,24 @@ constexpr int kTokenQuantum = 16;   // partition sizes are multiples of the warp
 #ifndef PA_SPLIT_OVERHEAD_BYTES
 #define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
 #endif
+// Work sharing among the splits of a sequence: each split keeps about
+// (1 - 1/kStealDiv) of its P tokens as a static share, and the rest of the context
+// is claimed tile by tile through one counter per (sequence, KV head) held in the
+// workspace header, for up to kStealUnits such pairs (beyond that, static splits)
+// and for splits that stream at least kStealMinBytes.
+#ifndef PA_STEAL_DIV
+#define PA_STEAL_DIV 8
+#endif
+constexpr int kStealDiv = PA_STEAL_DIV;
+// Shorter splits stay static: their imbalance costs less than a claim's round trip.
+#ifndef PA_STEAL_MIN_KIB
+#define PA_STEAL_MIN_KIB 512
+#endif
+constexpr long long kStealMinBytes = (long long)PA_STEAL_MIN_KIB * 1024;  // K + V bytes per split
+constexpr int kStealUnits = 2048;
+constexpr int kHeaderBytes = 256 + kStealUnits * 4;  // error word, then the counters
+static_assert(kHeaderBytes % 256 == 0, "header keeps 256-byte alignment");
+static_assert(kHeaderBytes == PA_WORKSPACE_HEADER_BYTES, "header size is part of the ABI");
 // A CTA's fixed cost (launch, first round trip, epilogue) expressed as the KV bytes
 // it could have streamed meanwhile; the split planner charges it once per CTA.
 constexpr int kSplitOverheadBytes = PA_SPLIT_OVERHEAD_BYTES;
@@ -31,9 +51,11 @@ struct DecodeParams {
   float* ws_l;        // [B*Hkv*S][G]   softmax denominator of each split
   float* ws_acc;      // [B*Hkv*S][G][D] unnormalised output of each split
   uint32_t* err;      // device error word
+  int* steal;         // [B*Hkv] claimed shared tiles per (sequence, KV head); zero between calls
   int B, Hq, Hkv, G;
   int block_size, num_blocks, max_blocks, max_seq_len;
   int S, P;           // splits and tokens per split
+  int Ps;             // static tokens per split (== P: no shared tiles)
   int window;         // > 0: attend to the last `window` tokens only
   int q_len;          // query rows per sequence (causal among themselves)
   int kv_fp8;         // caches hold FP8 E4M3 (k_scale is folded into scale_log2)

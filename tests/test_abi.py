@@ -78,6 +78,7 @@ def _call(lib, a, ws=256, nbytes=1 << 20):
     (dict(q_len=2, window=64), pa.PA_ERR_UNSUPPORTED),      # rows and a window: not both
     (dict(q_len=5, Hq=56, Hkv=8), pa.PA_ERR_UNSUPPORTED),   # 7 x 5 = 35 columns > 32
     (dict(q_len=3, Hq=48, Hkv=8, D=256), pa.PA_ERR_UNSUPPORTED),  # 18 columns > 16
+    (dict(flags=2), pa.PA_ERR_INVALID_ARG),                 # unknown flag bit
 ])
 def test_host_validation(lib, kw, code):
     assert _call(lib, _args(**kw)) == code
@@ -86,6 +87,26 @@ def test_host_validation(lib, kw, code):
 def test_workspace_checks_precede_cuda(lib):
     assert _call(lib, _args(), ws=0) == pa.PA_ERR_WORKSPACE
     assert _call(lib, _args(), ws=272) == pa.PA_ERR_WORKSPACE   # not 256-byte aligned
+
+
+def test_workspace_header(lib):
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    m = re.search(r"#define PA_WORKSPACE_HEADER_BYTES (\d+)u", src)
+    assert m and int(m.group(1)) == pa.PA_WORKSPACE_HEADER_BYTES
+    assert pa.PA_WORKSPACE_HEADER_BYTES % 256 == 0
+    # the header (error word + one tile counter per (sequence, KV head)) precedes the
+    # split partials, whatever the call's shape
+    import torch
+    if torch.cuda.is_available():  # sizes follow the current device's SM count
+        for B, Hkv, L in [(1, 8, 512), (1, 4, 32768), (64, 8, 32768)]:
+            need = lib.pa_decode_workspace_bytes(B, 2 * Hkv, Hkv, 128, 16, L)
+            assert need >= pa.PA_WORKSPACE_HEADER_BYTES
+    a = _args(flags=pa.PA_FLAG_DETERMINISTIC)
+    assert lib.pa_decode_ex_workspace_bytes(ctypes.byref(a)) == \
+        lib.pa_decode_ex_workspace_bytes(ctypes.byref(_args()))
+    # a workspace of exactly the header is too small for a call that splits
+    assert _call(lib, _args(max_seq_len=512), nbytes=pa.PA_WORKSPACE_HEADER_BYTES) in (
+        pa.PA_ERR_WORKSPACE, pa.PA_ERR_CUDA)
 
 
 def test_empty_batch_is_a_noop(lib):
