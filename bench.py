@@ -526,7 +526,7 @@ def run_ours(args, rank, world, local_rank):
             c.add_copies(max(1, min(256, -(-ROTATE_BYTES // max(1, c.kv_bytes())))))
             us = steady_state_us(pa, c, stream)
             gbs = c.kv_bytes() / (us * 1e-6) / 1e9
-            S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window)
+            S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8)
             entry = {"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
                      "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)}
             if len(members) == 16:  # the hybrid's 16 full-attention layers: one decode step
@@ -552,7 +552,7 @@ def run_ours(args, rank, world, local_rank):
             "timed": "CUDA graph of the whole step, replayed K times, CUDA events",
             "kv_bytes_per_step": kv}),
         "gpu_launches": sum(2 if pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len,
-                                         window=c.window)[0] > 1 else 1
+                                         window=c.window, kv_fp8=KV_FP8)[0] > 1 else 1
                             for c in cells) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,

@@ -263,9 +263,11 @@ def decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None,
 
 
 def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
-         splits: int = 0, sm_count: int = 0, window: int = 0) -> Tuple[int, int]:
+         splits: int = 0, sm_count: int = 0, window: int = 0,
+         kv_fp8: bool = False) -> Tuple[int, int]:
     """(splits, tokens per split) the library would launch with. sm_count <= 0 asks
-    the current device; a positive sm_count needs no GPU."""
+    the current device; a positive sm_count needs no GPU. kv_fp8: FP8 E4M3 caches
+    (their warp tile is 32 tokens, so splits are multiples of 32)."""
     lib = load()
     a = DecodeArgs()
     a.B, a.Hq, a.Hkv, a.D = B, Hq, Hkv, D
@@ -275,6 +277,8 @@ def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
     a.dtype = PA_BF16
     a.splits = splits
     a.window = window
+    if kv_fp8:
+        a.kv_dtype, a.k_scale, a.v_scale = PA_KV_FP8_E4M3, 1.0, 1.0
     S, P = ctypes.c_int(0), ctypes.c_int(0)
     rc = lib.pa_decode_plan(ctypes.byref(a), int(sm_count), ctypes.byref(S), ctypes.byref(P))
     if rc != PA_OK:

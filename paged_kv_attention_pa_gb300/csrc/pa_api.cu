@@ -20,7 +20,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------- split plan
 // Choose S (splits of each sequence's context) and P (tokens per split, a
-// multiple of the 16-token warp tile). The unit of parallel work is a (sequence,
+// multiple of the warp tile: 16 tokens, 32 for fp8 caches, so that no tile
+// crosses from one split's tokens into the next). The unit of parallel work is a (sequence,
 // KV head, split) CTA, one resident per SM. The cost of a plan is the number of
 // CTA waves times the tokens a CTA streams plus its fixed cost; candidates are
 // one split and the largest split counts that fill exactly 1..4 waves.
@@ -29,13 +30,14 @@ struct Plan {
   int P;
 };
 
-bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, Plan* out) {
-  int64_t P = round_up(ceil_div(max_len, std::max<int64_t>(S_req, 1)), pa::kTokenQuantum);
+bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, int64_t quantum,
+              Plan* out) {
+  int64_t P = round_up(ceil_div(max_len, std::max<int64_t>(S_req, 1)), quantum);
   if (floor_p) P = std::max<int64_t>(P, pa::kPartitionMin);
   P = std::min(P, p_max);
   int64_t S = ceil_div(max_len, P);
   if (S > pa::kMaxSplits) {
-    P = round_up(ceil_div(max_len, pa::kMaxSplits), pa::kTokenQuantum);
+    P = round_up(ceil_div(max_len, pa::kMaxSplits), quantum);
     if (P > p_max) return false;  // context too long for this block size
     S = ceil_div(max_len, P);
   }
@@ -44,16 +46,16 @@ bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, Plan*
 }
 
 bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_size,
-               int64_t max_len, int requested, Plan* out) {
+               int64_t max_len, int requested, int64_t quantum, Plan* out) {
   if (max_len <= 0) {
-    *out = {1, pa::kTokenQuantum};
+    *out = {1, (int)quantum};
     return true;
   }
   const int64_t units = B * Hkv;
   const int64_t sm = sm_count > 0 ? sm_count : 1;
   (void)block_size;
-  const int64_t p_max = round_up(max_len, pa::kTokenQuantum);
-  if (requested > 0) return plan_for(requested, max_len, p_max, false, out);
+  const int64_t p_max = round_up(max_len, quantum);
+  if (requested > 0) return plan_for(requested, max_len, p_max, false, quantum, out);
   bool found = false;
   int64_t best_cost = 0;
   const int64_t cands[6] = {1, sm / units, 2 * sm / units, 3 * sm / units, 4 * sm / units,
@@ -61,7 +63,7 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
   for (int64_t c : cands) {
     if (c < 1) continue;
     Plan pl{};
-    if (!plan_for(c, max_len, p_max, true, &pl)) continue;
+    if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
     const int64_t waves = ceil_div(units * pl.S, sm);
     const int64_t overhead_tokens = pa::kSplitOverheadBytes / (4 * D);  // K + V bytes per token
     const int64_t cost = waves * (pl.P + overhead_tokens);
@@ -150,6 +152,11 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   return PA_OK;
 }
 
+// Tokens per warp tile of the kernel that serves these arguments.
+int64_t tile_tokens(const pa_decode_args* a) {
+  return a->kv_dtype == PA_KV_FP8_E4M3 ? 2 * pa::kTokenQuantum : pa::kTokenQuantum;
+}
+
 // Tokens one sequence's splits must cover: a sliding window bounds them.
 int64_t plan_len(const pa_decode_args* a, int64_t max_len) {
   return (a->window > 0 && a->window < max_len) ? a->window : max_len;
@@ -193,7 +200,7 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
   if (sm_count <= 0) return PA_ERR_CUDA;
   Plan plan{};
   if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
-                 &plan))
+                 tile_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   *splits = plan.S;
   *partition_tokens = plan.P;
@@ -262,7 +269,8 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const int sm = current_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits, &plan))
+  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
+                 tile_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const int rows = a->q_len > 0 ? a->q_len : 1;
@@ -296,7 +304,8 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const long long split_bytes = (long long)plan.P * 2 * a->D * (a->kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2);
   if (plan.S > 1 && !(a->flags & PA_FLAG_DETERMINISTIC) && pa::kStealDiv > 0 &&
       split_bytes >= pa::kStealMinBytes && (int64_t)a->B * a->Hkv <= pa::kStealUnits) {
-    const int shared = (plan.P / pa::kStealDiv) / pa::kTokenQuantum * pa::kTokenQuantum;
+    const int tw = (int)tile_tokens(a);  // static shares stay whole tiles
+    const int shared = (plan.P / pa::kStealDiv) / tw * tw;
     p.Ps = plan.P - shared;
   }
   p.steal = reinterpret_cast<int*>(ws + 256);

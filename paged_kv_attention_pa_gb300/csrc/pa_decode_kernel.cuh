@@ -46,33 +46,31 @@
 namespace pa {
 
 constexpr int kSmemBudget = 224 * 1024;
-constexpr int kTileTokens = 16;  // M of the score MMA
+constexpr int kTileTokens = 16;  // M of the score MMA (fp8 tiles hold two row blocks)
 
 // F8: the cache holds FP8 E4M3 (one byte per element); tiles land in the ring as
-// bytes and each warp widens its tile into an fp16 staging tile for the MMAs.
+// bytes, and each lane widens the bytes of its MMA fragments in registers.
 template <int D, int NT, bool F8 = false>
 struct Cfg {
   static constexpr int NW = D == 128 ? PA_WARPS_D128 : PA_WARPS_D256;  // warps per CTA
   static constexpr int THREADS = NW * 32;
-  static constexpr int TW = kTileTokens;
+  static constexpr int TW = F8 ? 2 * kTileTokens : kTileTokens;  // tokens per tile
   static constexpr int GT = 8 * NT;             // heads computed (G padded)
   static constexpr int KVB = F8 ? 1 : 2;        // bytes per cache element
   static constexpr int ROWB = D * KVB + 16;     // ring row pitch, padded against bank conflicts
-  static constexpr int ROWB_M = D * 2 + 16;     // MMA-operand row pitch (16-bit elements)
   static constexpr int CPR = D * KVB / 16;      // 16-byte chunks per row
   static constexpr int TILE_BYTES = TW * ROWB;  // K (or V) half of a slot
   static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
-  static constexpr int STAGE_BYTES = F8 ? TW * ROWB_M : 0;  // per warp, V only (fp8 only)
   static constexpr int KS = D / 16;             // k-steps of the score MMA = d-blocks of PV
   static constexpr int COPIES = TW * CPR / 32;  // 16-byte copies per lane per operand per tile
   static constexpr int FIXED = 256;
-  static constexpr int DEPTH_FIT = (kSmemBudget - FIXED - NW * STAGE_BYTES) / (NW * SLOT_BYTES);
+  static constexpr int DEPTH_FIT = (kSmemBudget - FIXED) / (NW * SLOT_BYTES);
   static constexpr int DEPTH = DEPTH_FIT > 12 ? 12 : DEPTH_FIT;  // slots per warp
   static constexpr int RING = NW * DEPTH * SLOT_BYTES;
-  static constexpr int SMEM = RING + NW * STAGE_BYTES + FIXED;
+  static constexpr int SMEM = RING + FIXED;
   static_assert((TW * CPR) % 32 == 0, "tile shape");
   static_assert(DEPTH >= 2, "need at least two slots per warp");
-  static_assert(NW * GT * (D + 6) * 4 <= RING + NW * STAGE_BYTES, "CTA merge must fit");
+  static_assert(NW * GT * (D + 6) * 4 <= RING, "CTA merge must fit");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
@@ -166,10 +164,11 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk) {
         // fp8 caches feed K to the MMA in a permuted d order: fragment elements
-        // {2tig, 2tig+1, 2tig+8, 2tig+9} of k-step kk hold d = 16kk + 4tig + {0,1,2,3};
-        // q takes the same order, so every dot product is unchanged.
-        const int i0 = F8 ? kk * 8 + 2 * tig : kk * 8 + tig;
-        const int i1 = F8 ? kk * 8 + 2 * tig + 1 : kk * 8 + 4 + tig;
+        // {2tig, 2tig+1, 2tig+8, 2tig+9} of k-step kk hold d = 4 KS tig + 4kk + {0..3},
+        // so that a lane's K bytes of a row are contiguous; q takes the same order and
+        // every dot product is unchanged.
+        const int i0 = F8 ? 2 * C::KS * tig + 2 * kk : kk * 8 + tig;
+        const int i1 = F8 ? 2 * C::KS * tig + 2 * kk + 1 : kk * 8 + 4 + tig;
         qf[nt][kk][0] = ok ? __ldg(q32 + rowp + i0) : 0u;
         qf[nt][kk][1] = ok ? __ldg(q32 + rowp + i1) : 0u;
         if constexpr (F8 && !std::is_same_v<T, __half>) {  // queries as fp16 pairs
@@ -327,10 +326,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 #pragma unroll
     for (int dd = 0; dd < C::KS; ++dd) o[nt][dd][0] = o[nt][dd][1] = o[nt][dd][2] = o[nt][dd][3] = 0.f;
   }
-  // ldmatrix row addresses (byte offsets inside a tile) for this lane
-  const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB_M + (lane >> 4) * 16);
-  const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB_M + ((lane >> 3) & 1) * 16);
-  uint8_t* my_stage = ring + C::RING + warp * C::STAGE_BYTES;  // fp8 only
+  // ldmatrix row addresses (byte offsets inside a 16-bit tile) for this lane
+  const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB + (lane >> 4) * 16);
+  const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB + ((lane >> 3) & 1) * 16);
   const float sl2 = p.scale_log2;
 
   for (int k = 0; tq[0] >= 0; ++k) {  // tile k of the stream: tokens tq[0] ..
@@ -344,35 +342,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     for (int i = 0; i + 1 < C::DEPTH; ++i) tq[i] = tq[i + 1];
     tq[C::DEPTH - 1] = t_new;
     const int nv = min(C::TW, L - t0);
-    uint32_t kt, vt;
-    if constexpr (F8) {
-      // widen this tile's V bytes to fp16 in the warp's staging tile (the PV MMA reads
-      // V transposed); rows past seq_len (never loaded) become zeros, so that p = 0
-      // meets 0 in the PV sum. K stays in the ring: the score MMA widens it in
-      // registers.
-      __syncwarp();  // every lane's copies have landed
-      const uint8_t* slot = my_ring + (k % C::DEPTH) * C::SLOT_BYTES;
-#pragma unroll
-      for (int i = 0; i < C::COPIES; ++i) {
-        const int flat = i * 32 + lane;
-        const int r = flat / C::CPR, c = flat % C::CPR;
-        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-        if (r < nv) {
-          const uint4 w = *reinterpret_cast<const uint4*>(slot + C::TILE_BYTES + r * C::ROWB + c * 16);
-          lo = make_uint4(e4m3x2_to_half2(w.x & 0xffff), e4m3x2_to_half2(w.x >> 16),
-                          e4m3x2_to_half2(w.y & 0xffff), e4m3x2_to_half2(w.y >> 16));
-          hi = make_uint4(e4m3x2_to_half2(w.z & 0xffff), e4m3x2_to_half2(w.z >> 16),
-                          e4m3x2_to_half2(w.w & 0xffff), e4m3x2_to_half2(w.w >> 16));
-        }
-        uint8_t* dst = my_stage + r * C::ROWB_M + c * 32;
-        *reinterpret_cast<uint4*>(dst) = lo;
-        *reinterpret_cast<uint4*>(dst + 16) = hi;
-      }
-      kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
-      vt = smem_addr(my_stage);
-    } else {
-      kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
-      vt = kt + C::TILE_BYTES;
+    const uint32_t kt = my_ring_s + (k % C::DEPTH) * C::SLOT_BYTES;
+    const uint32_t vt = kt + C::TILE_BYTES;
+    if constexpr (!F8) {
       if (nv < C::TW) {
         // rows past seq_len were never loaded: zero them in V so that p = 0 meets 0
         uint8_t* vrow = my_ring + (k % C::DEPTH) * C::SLOT_BYTES + C::TILE_BYTES;
@@ -384,55 +356,73 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     }
     __syncwarp();  // every lane's copies (and the zero rows) are visible
 
-    // ---- scores S^T[token][head] = K_tile . q^T (fp32 accumulate)
-    // two independent accumulator chains (even / odd k-steps) halve the MMA latency
-    float s[NT][4], s2[NT][4];
+    // ---- scores S^T[token][head] = K_tile . q^T (fp32 accumulate), one MMA row
+    // block per 16 tokens (mt); two independent accumulator chains (even / odd
+    // k-steps) halve the MMA latency
+    constexpr int MT = C::TW / 16;
+    float s[MT][NT][4], s2[MT][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int kk = 0; kk < C::KS; ++kk) {
-      uint32_t a[4];
-      if constexpr (F8) {
-        // rows gid and gid + 8, d = 16kk + 4tig .. +3: four e4m3 bytes each
-        uint32_t w0, w1;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(kt + gid * C::ROWB + kk * 16 + 4 * tig));
-        asm volatile("ld.shared.u32 %0, [%1];"
-                     : "=r"(w1)
-                     : "r"(kt + (gid + 8) * C::ROWB + kk * 16 + 4 * tig));
-        a[0] = e4m3x2_to_half2(w0 & 0xffff);
-        a[2] = e4m3x2_to_half2(w0 >> 16);
-        a[1] = e4m3x2_to_half2(w1 & 0xffff);
-        a[3] = e4m3x2_to_half2(w1 >> 16);
-      } else {
-        ldmatrix_x4<false>(a, kt + k_lane + kk * 32);
-      }
+        for (int i = 0; i < 4; ++i) s[mt][nt][i] = s2[mt][nt][i] = 0.f;
+    // fp8: this lane's K bytes d in [4 KS tig, 4 KS tig + 4 KS) of rows 16mt + gid and
+    // 16mt + gid + 8 (rows past seq_len hold stale bytes: their scores become -inf)
+    uint4 kw[MT][2][F8 ? C::KS / 4 : 1];
+    if constexpr (F8) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (kk & 1)
-          mma16816<TM>(s2[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-        else
-          mma16816<TM>(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-      }
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int u = 0; u < C::KS / 4; ++u) {
+          kw[mt][0][u] = lds128(kt + (16 * mt + gid) * C::ROWB + 4 * C::KS * tig + 16 * u);
+          kw[mt][1][u] = lds128(kt + (16 * mt + gid + 8) * C::ROWB + 4 * C::KS * tig + 16 * u);
+        }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int kk = 0; kk < C::KS; ++kk) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
-    // tokens gid and gid + 8 of the tile; -inf by select past each column's limit
-    // (seq_len, and the causal limit of the column's query row); rows past seq_len
-    // were never loaded
-    const int tok0 = t0 + gid, tok1 = tok0 + 8;
-    uint32_t pb[NT][2];
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a[4];
+        if constexpr (F8) {
+          // k-step kk: d = 4 KS tig + 4kk .. +3 of the two rows
+          const uint32_t w0 = word_of(kw[mt][0][kk / 4], kk % 4);
+          const uint32_t w1 = word_of(kw[mt][1][kk / 4], kk % 4);
+          a[0] = e4m3x2_to_half2(w0 & 0xffff);
+          a[2] = e4m3x2_to_half2(w0 >> 16);
+          a[1] = e4m3x2_to_half2(w1 & 0xffff);
+          a[3] = e4m3x2_to_half2(w1 >> 16);
+        } else {
+          ldmatrix_x4<false>(a, kt + 16 * mt * C::ROWB + k_lane + kk * 32);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (kk & 1)
+            mma16816<TM>(s2[mt][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+          else
+            mma16816<TM>(s[mt][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+      }
+    }
+    // ---- online softmax over the tile. Tokens 16mt + gid (+ 8); -inf by select past
+    // each column's limit (seq_len, and the causal limit of the column's query row);
+    // rows past seq_len were never loaded
+    uint32_t pb[MT][NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float x0 = tok0 < lim[nt][0] ? s[nt][0] * sl2 : -INFINITY;
-      float x1 = tok0 < lim[nt][1] ? s[nt][1] * sl2 : -INFINITY;
-      float x2 = tok1 < lim[nt][0] ? s[nt][2] * sl2 : -INFINITY;
-      float x3 = tok1 < lim[nt][1] ? s[nt][3] * sl2 : -INFINITY;
-      // tile max per head over the 16 tokens (lanes sharing tig)
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      float x[MT][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int tok0 = t0 + 16 * mt + gid, tok1 = tok0 + 8;
+        x[mt][0] = tok0 < lim[nt][0] ? (s[mt][nt][0] + s2[mt][nt][0]) * sl2 : -INFINITY;
+        x[mt][1] = tok0 < lim[nt][1] ? (s[mt][nt][1] + s2[mt][nt][1]) * sl2 : -INFINITY;
+        x[mt][2] = tok1 < lim[nt][0] ? (s[mt][nt][2] + s2[mt][nt][2]) * sl2 : -INFINITY;
+        x[mt][3] = tok1 < lim[nt][1] ? (s[mt][nt][3] + s2[mt][nt][3]) * sl2 : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(x[mt][0], x[mt][2]));
+        mx1 = fmaxf(mx1, fmaxf(x[mt][1], x[mt][3]));
+      }
+      // tile max per head over its tokens (lanes sharing tig)
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
@@ -443,10 +433,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       const float al0 = exp2f(m[nt][0] - r0), al1 = exp2f(m[nt][1] - r1);
       m[nt][0] = mn0;
       m[nt][1] = mn1;
-      const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1);
-      const float p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
-      l[nt][0] = l[nt][0] * al0 + p0 + p2;
-      l[nt][1] = l[nt][1] * al1 + p1 + p3;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const float p0 = exp2f(x[mt][0] - r0), p1 = exp2f(x[mt][1] - r1);
+        const float p2 = exp2f(x[mt][2] - r0), p3 = exp2f(x[mt][3] - r1);
+        ps0 += p0 + p2;
+        ps1 += p1 + p3;
+        // P^T[token][head] fragments -> P[head][token] as the B operand of PV
+        pb[mt][nt][0] = movmatrix_trans(pack2<TM>(p0, p1));
+        pb[mt][nt][1] = movmatrix_trans(pack2<TM>(p2, p3));
+      }
+      l[nt][0] = l[nt][0] * al0 + ps0;
+      l[nt][1] = l[nt][1] * al1 + ps1;
 #pragma unroll
       for (int dd = 0; dd < C::KS; ++dd) {
         o[nt][dd][0] *= al0;
@@ -454,18 +453,57 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         o[nt][dd][2] *= al0;
         o[nt][dd][3] *= al1;
       }
-      // P^T[token][head] fragments -> P[head][token] as the B operand of PV
-      pb[nt][0] = movmatrix_trans(pack2<TM>(p0, p1));
-      pb[nt][1] = movmatrix_trans(pack2<TM>(p2, p3));
     }
 
-    // ---- O^T[d][head] += V_tile^T . P^T
+    // ---- O^T[d][head] += V_tile^T . P^T, one MMA per d-block and row block
+    if constexpr (F8) {
+      // Rows of the V^T fragments are permuted: in d-block dd, row gid holds
+      // d = 2 KS gid + 2dd and row gid + 8 holds d + 1, so that a lane needs bytes
+      // [2 KS gid, 2 KS gid + 2 KS) of its tokens 16mt + {2tig, 2tig+1, 2tig+8,
+      // 2tig+9}: one or two 16-byte loads per token, then a byte permute pairs two
+      // tokens of one d for each fp16x2 register. Rows past seq_len read as 0.
+      uint4 vw[MT][4][C::KS / 8];
 #pragma unroll
-    for (int dd = 0; dd < C::KS; ++dd) {
-      uint32_t a[4];
-      ldmatrix_x4<true>(a, vt + v_lane + dd * 32);
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<TM>(o[nt][dd], a, pb[nt][0], pb[nt][1]);
+        for (int j = 0; j < 4; ++j) {
+          const int r = 16 * mt + 2 * tig + (j & 1) + 8 * (j >> 1);
+#pragma unroll
+          for (int u = 0; u < C::KS / 8; ++u) {
+            const uint4 x = lds128(vt + r * C::ROWB + 2 * C::KS * gid + 16 * u);
+            vw[mt][j][u] = r < nv ? x : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+      for (int dd = 0; dd < C::KS; ++dd) {
+        const int wi = dd >> 1;                             // word of bytes 2dd, 2dd + 1
+        const uint32_t sel = (dd & 1) ? 0x7362u : 0x5140u;  // pair bytes 2,3 or 0,1
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t p01 = __byte_perm(word_of(vw[mt][0][wi / 4], wi % 4),
+                                           word_of(vw[mt][1][wi / 4], wi % 4), sel);
+          const uint32_t p23 = __byte_perm(word_of(vw[mt][2][wi / 4], wi % 4),
+                                           word_of(vw[mt][3][wi / 4], wi % 4), sel);
+          uint32_t a[4];
+          a[0] = e4m3x2_to_half2(p01 & 0xffff);  // row gid:     tokens 2tig, 2tig+1
+          a[1] = e4m3x2_to_half2(p01 >> 16);     // row gid + 8: tokens 2tig, 2tig+1
+          a[2] = e4m3x2_to_half2(p23 & 0xffff);  // row gid:     tokens 2tig+8, 2tig+9
+          a[3] = e4m3x2_to_half2(p23 >> 16);     // row gid + 8: tokens 2tig+8, 2tig+9
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<TM>(o[nt][dd], a, pb[mt][nt][0], pb[mt][nt][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int dd = 0; dd < C::KS; ++dd) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a[4];
+          ldmatrix_x4<true>(a, vt + 16 * mt * C::ROWB + v_lane + dd * 32);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<TM>(o[nt][dd], a, pb[mt][nt][0], pb[mt][nt][1]);
+        }
+      }
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
   }
@@ -517,11 +555,13 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     float* a0 = aw + (warp * GT + c0) * AP;
 #pragma unroll
     for (int dd = 0; dd < C::KS; ++dd) {
-      const int d0 = dd * 16 + gid;
-      a0[d0] = o[nt][dd][0] * f[0];
-      a0[AP + d0] = o[nt][dd][1] * f[1];
-      a0[d0 + 8] = o[nt][dd][2] * f[0];
-      a0[AP + d0 + 8] = o[nt][dd][3] * f[1];
+      // rows gid and gid + 8 of d-block dd (permuted for fp8 caches, see the PV step)
+      const int dlo = F8 ? 2 * C::KS * gid + 2 * dd : dd * 16 + gid;
+      const int dhi = F8 ? dlo + 1 : dlo + 8;
+      a0[dlo] = o[nt][dd][0] * f[0];
+      a0[AP + dlo] = o[nt][dd][1] * f[1];
+      a0[dhi] = o[nt][dd][2] * f[0];
+      a0[AP + dhi] = o[nt][dd][3] * f[1];
     }
   }
   __syncthreads();

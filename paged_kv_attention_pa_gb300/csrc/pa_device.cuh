@@ -35,6 +35,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
   return y;
 }
 
+// 16-byte shared-memory load from a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// Word i (0..3) of a 16-byte vector; i is a constant after unrolling.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // ---------------------------------------------------------------- dependent launch
 // Wait until the grids this one depends on (programmatic launch) have completed
 // and their writes are visible; returns at once for an ordinary launch.

@@ -14,7 +14,7 @@ namespace pa {
 // bytes at any context length.
 constexpr int kMaxSplits = 1024;
 constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost dominates
-constexpr int kTokenQuantum = 16;   // partition sizes are multiples of the warp tile
+constexpr int kTokenQuantum = 16;   // warp tile (32 for fp8 caches); partitions are whole tiles
 #ifndef PA_SPLIT_OVERHEAD_BYTES
 #define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
 #endif
