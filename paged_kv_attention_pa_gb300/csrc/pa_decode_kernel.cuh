@@ -6,21 +6,27 @@
 // split-KV fix of the same page so that B * Hkv * splits fills every SM even at
 // batch 1 with 4 KV heads).
 //
-// Loads. Every warp streams its own 16-token tiles (tile j goes to warp j % NW)
-// through a private ring of DEPTH shared-memory slots with 16-byte cp.async
-// copies (L2 evict-first), DEPTH - 1 tiles in flight while it computes one: per
-// warp pipelines keep ~140-170 KB of loads in flight per SM. Only rows of live
+// Loads. Every warp streams its own tiles of TW tokens (32 at head_dim 128 and
+// for fp8 caches, 16 at head_dim 256) through a private ring of DEPTH shared-memory
+// slots with 16-byte cp.async copies (L2 evict-first), DEPTH - 1 tiles in flight
+// while it computes one: ~130-160 KB of loads in flight per SM. A warp's tiles are
+// first those of its split's static share (tile j to warp j % NW), then tiles of
+// the sequence's shared tail, claimed one at a time from a counter per (sequence,
+// KV head), so that splits on faster SMs stream more of them. Only rows of live
 // tokens (t < seq_len) are copied; the unwritten tail of the last block is never
 // read ("vLLM's custom ROCm paged-attention kernel wins all sixty cells", §5,
-// the V-load fault), and V rows of a partial tile are zeroed in shared memory so
-// that the tensor-core sum over tokens only ever sees finite values there.
+// the V-load fault), and V rows past seq_len are zeroed (in shared memory, or in
+// registers for fp8) so that the tensor-core sum over tokens only sees finite
+// values there.
 //
 // Math. The GQA group's two contractions run on tensor cores per warp
-// (mma.sync m16n8k16, fp32 accumulate): S^T[16 tokens x 8 heads] = K_tile q^T,
-// then O^T[d x 8 heads] += V_tile^T P^T with P rounded to the input type. Scores
-// of tokens past seq_len become -inf by select before the online softmax (exp2
-// domain, running max and sum per head). Groups of 9..16 heads use two 8-head
-// column tiles.
+// (mma.sync m16n8k16, fp32 accumulate), one MMA row block per 16 tokens:
+// S^T[16 tokens x 8 heads] = K_tile q^T, then O^T[d x 8 heads] += V_tile^T P^T with
+// P rounded to the MMA type. Scores of tokens past seq_len become -inf by select
+// before the online softmax (exp2 domain, running max and sum per head). Groups
+// of 9..16 heads (or query rows x heads) use two or four 8-column tiles. FP8 E4M3
+// K and V bytes are widened exactly to fp16 in registers, straight into the MMA
+// fragments.
 //
 // Epilogue: the warps merge their (m, l, acc) in shared memory. A sequence that
 // fits in one split gets its output written here; otherwise the split's partial
@@ -37,24 +43,27 @@
 #include "pa_params.h"
 
 #ifndef PA_WARPS_D128
-#define PA_WARPS_D128 8
+#define PA_WARPS_D128 4
 #endif
 #ifndef PA_WARPS_D256
 #define PA_WARPS_D256 4
+#endif
+#ifndef PA_WARPS_F8_D128
+#define PA_WARPS_F8_D128 8  // fp8 tiles cost more math per byte: more warps
 #endif
 
 namespace pa {
 
 constexpr int kSmemBudget = 224 * 1024;
-constexpr int kTileTokens = 16;  // M of the score MMA (fp8 tiles hold two row blocks)
 
 // F8: the cache holds FP8 E4M3 (one byte per element); tiles land in the ring as
 // bytes, and each lane widens the bytes of its MMA fragments in registers.
 template <int D, int NT, bool F8 = false>
 struct Cfg {
-  static constexpr int NW = D == 128 ? PA_WARPS_D128 : PA_WARPS_D256;  // warps per CTA
+  static constexpr int NW = D == 128 ? (F8 ? PA_WARPS_F8_D128 : PA_WARPS_D128) : PA_WARPS_D256;  // warps
   static constexpr int THREADS = NW * 32;
-  static constexpr int TW = F8 ? 2 * kTileTokens : kTileTokens;  // tokens per tile
+  static constexpr int TW = F8 ? kTileTokensF8 : tile_tokens_16bit(D);  // tokens per tile
+  static_assert(TW % 16 == 0 && TW <= 32, "a tile is whole MMA row blocks, one token per lane");
   static constexpr int GT = 8 * NT;             // heads computed (G padded)
   static constexpr int KVB = F8 ? 1 : 2;        // bytes per cache element
   static constexpr int ROWB = D * KVB + 16;     // ring row pitch, padded against bank conflicts

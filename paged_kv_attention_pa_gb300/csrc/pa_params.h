@@ -14,7 +14,17 @@ namespace pa {
 // bytes at any context length.
 constexpr int kMaxSplits = 1024;
 constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost dominates
-constexpr int kTokenQuantum = 16;   // warp tile (32 for fp8 caches); partitions are whole tiles
+// Tokens per warp tile (a multiple of the score MMA's 16 rows); split partitions
+// and static shares are whole tiles.
+#ifndef PA_TILE_TOKENS_D128
+#define PA_TILE_TOKENS_D128 32
+#endif
+#ifndef PA_TILE_TOKENS_D256
+#define PA_TILE_TOKENS_D256 16
+#endif
+// bf16 / fp16 caches: per head_dim (a 256-wide row pair is already 1 KB a token)
+constexpr int tile_tokens_16bit(int D) { return D == 128 ? PA_TILE_TOKENS_D128 : PA_TILE_TOKENS_D256; }
+constexpr int kTileTokensF8 = 32;  // fp8 caches (half the bytes per token)
 #ifndef PA_SPLIT_OVERHEAD_BYTES
 #define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
 #endif

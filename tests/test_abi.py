@@ -157,8 +157,14 @@ def test_forced_splits():
     for want in (1, 2, 3, 7):
         S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=want, sm_count=SM)
         assert S == want and S * P >= 1025
+    # the finest split is one warp tile: 32 tokens at head_dim 128 and for fp8
+    # caches, 16 at head_dim 256
     S, P = pa.plan(1, 16, 8, 128, 16, 1025, splits=10000, sm_count=SM)
+    assert P == 32 and S == 33
+    S, P = pa.plan(1, 16, 8, 256, 16, 1025, splits=10000, sm_count=SM)
     assert P == 16 and S == 65
+    S, P = pa.plan(1, 16, 8, 256, 16, 1025, splits=10000, sm_count=SM, kv_fp8=True)
+    assert P == 32 and S == 33
 
 
 def test_large_batch_needs_no_split():
