@@ -237,6 +237,50 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# DRAM traffic of decode_kernel per algorithmic KV byte, from ncu captures of single
+# cells (dram__bytes_read.sum + dram__bytes_write.sum, mean over the captured
+# launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
+# A capture holds only for the kernel sources it was taken on: when their SHA-256
+# differs from the one recorded here, the bench reports traffic as null.
+TRAFFIC_SOURCES_SHA256 = "b3705c8c009660fbd32d0d7c9914796b0db83feba507db354d8288dc0f796253"
+TRAFFIC_CAPTURES = {
+    # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
+    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537048064 + 984661},
+    # 24q/4kv, block 784, batch 1, 32768 tokens: two launches
+    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134301056 + 3026944},
+    # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: two launches
+    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268604544 + 2941568},
+}
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_attention_pa_gb300", "csrc")
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "pa.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_per_call(alg_bytes_per_call: float, D: int, kv: str):
+    """(bytes, note): DRAM bytes of one decode call scaled from the matching capture,
+    or (None, why)."""
+    cap = TRAFFIC_CAPTURES.get((D, kv))
+    if cap is None:
+        return None, f"no ncu capture for head_dim {D}, {kv} KV"
+    if kernel_sources_sha256() != TRAFFIC_SOURCES_SHA256:
+        return None, "kernel sources changed since the ncu capture"
+    ratio = cap["dram_bytes"] / cap["alg_bytes"]
+    return round(alg_bytes_per_call * ratio), (
+        f"ncu dram bytes / algorithmic bytes = {ratio:.5f} on a head_dim {D} {kv} cell, "
+        "scaled by the call's KV bytes")
+
+
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -538,6 +582,10 @@ def run_ours(args, rank, world, local_rank):
     budget = float(os.environ.get("PA_BENCH_CPU_BUDGET_S", "12"))
     cb_bytes, cb_s, cb_desc = oracle_sample(budget, device=dev)
     achieved = alg / (ms_step_max * 1e-3) / 1e9
+    Ds = {c.D for c in cells}
+    traffic, traffic_note = (traffic_per_call(alg / len(cells), Ds.pop(),
+                                              "fp8" if KV_FP8 else "bf16")
+                             if len(Ds) == 1 else (None, "cells of several head_dims"))
     line = {
         "impl": "ours", "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -555,7 +603,8 @@ def run_ours(args, rank, world, local_rank):
                                          window=c.window, kv_fp8=KV_FP8)[0] > 1 else 1
                             for c in cells) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_source": traffic_note,
                      "peak_kind": peak_kind,
                      "kernel": "pa::decode_kernel (+ pa::merge_kernel when split)",
                      "alg_bytes_per_launch": round(alg / len(cells)),
