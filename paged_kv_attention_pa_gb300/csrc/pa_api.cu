@@ -154,7 +154,7 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
 
 // Tokens per warp tile of the kernel that serves these arguments.
 int64_t tile_tokens(const pa_decode_args* a) {
-  return a->kv_dtype == PA_KV_FP8_E4M3 ? pa::kTileTokensF8 : pa::tile_tokens_16bit(a->D);
+  return pa::tile_tokens(a->D, a->kv_dtype == PA_KV_FP8_E4M3);
 }
 
 // Tokens one sequence's splits must cover: a sliding window bounds them.

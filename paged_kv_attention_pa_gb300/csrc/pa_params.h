@@ -22,9 +22,18 @@ constexpr int kPartitionMin = 64;   // tokens: below this a split's fixed cost d
 #ifndef PA_TILE_TOKENS_D256
 #define PA_TILE_TOKENS_D256 16
 #endif
-// bf16 / fp16 caches: per head_dim (a 256-wide row pair is already 1 KB a token)
-constexpr int tile_tokens_16bit(int D) { return D == 128 ? PA_TILE_TOKENS_D128 : PA_TILE_TOKENS_D256; }
-constexpr int kTileTokensF8 = 32;  // fp8 caches (half the bytes per token)
+#ifndef PA_TILE_TOKENS_F8_D128
+#define PA_TILE_TOKENS_F8_D128 32
+#endif
+#ifndef PA_TILE_TOKENS_F8_D256
+#define PA_TILE_TOKENS_F8_D256 32
+#endif
+// Per head_dim and cache type: a 256-wide 16-bit row pair is already 1 KB a token;
+// fp8 rows carry half the bytes of a 16-bit row for the same arithmetic.
+constexpr int tile_tokens(int D, bool fp8) {
+  return fp8 ? (D == 128 ? PA_TILE_TOKENS_F8_D128 : PA_TILE_TOKENS_F8_D256)
+             : (D == 128 ? PA_TILE_TOKENS_D128 : PA_TILE_TOKENS_D256);
+}
 #ifndef PA_SPLIT_OVERHEAD_BYTES
 #define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
 #endif

@@ -247,7 +247,7 @@ def tile_index_case(B, hq, hkv, D, bs, lens, R=1, dtype="bf16", kv_dtype=None, s
     return case
 
 
-def tile_index_expected(lens, R, hq, hkv, D):
+def tile_index_expected(lens, R, hq, hkv, D, window=0):
     B, G = len(lens), hq // hkv
     e = np.zeros((B, R, hq, D))
     for b, L in enumerate(lens):
@@ -255,28 +255,30 @@ def tile_index_expected(lens, R, hq, hkv, D):
             Lr = L - R + i + 1
             if Lr <= 0:
                 continue
-            t = np.arange(Lr)
+            t = np.arange(max(0, Lr - window) if window else 0, Lr)
+            Lr = len(t)
             for h in range(hq):
                 e[b, i, h] = np.bincount((t // 16 + h // G) % D, minlength=D) / Lr
     return e if R > 1 else e[:, 0]
 
 
-@pytest.mark.parametrize("B,hq,hkv,D,bs,lens,R,dtype,kv,splits", [
-    (1, 8, 8, 128, 16, [32768], 1, "bf16", None, 0),
-    (1, 8, 8, 128, 16, [32763], 1, "f16", None, 0),        # ragged last tile
-    (1, 24, 4, 256, 784, [32768], 1, "bf16", None, 0),
-    (2, 16, 8, 128, 16, [32768, 20000], 1, "f16", None, 0),  # shorter second sequence
-    (1, 8, 8, 128, 16, [65536], 1, "bf16", "fp8", 0),
-    (1, 32, 8, 128, 16, [32768], 4, "bf16", None, 0),      # four causal query rows
-    (1, 8, 8, 128, 16, [32768], 1, "bf16", None, 2),       # two long splits
-    (1, 24, 4, 256, 784, [9000], 1, "bf16", None, 5),
+@pytest.mark.parametrize("B,hq,hkv,D,bs,lens,R,dtype,kv,splits,window", [
+    (1, 8, 8, 128, 16, [32768], 1, "bf16", None, 0, 0),
+    (1, 8, 8, 128, 16, [32763], 1, "f16", None, 0, 0),        # ragged last tile
+    (1, 24, 4, 256, 784, [32768], 1, "bf16", None, 0, 0),
+    (2, 16, 8, 128, 16, [32768, 20000], 1, "f16", None, 0, 0),  # shorter second sequence
+    (1, 8, 8, 128, 16, [65536], 1, "bf16", "fp8", 0, 0),
+    (1, 32, 8, 128, 16, [32768], 4, "bf16", None, 0, 0),      # four causal query rows
+    (1, 8, 8, 128, 16, [32768], 1, "bf16", None, 2, 0),       # two long splits
+    (1, 24, 4, 256, 784, [9000], 1, "bf16", None, 5, 0),
+    (2, 8, 8, 128, 16, [32768, 30001], 1, "bf16", None, 0, 30000),  # sliding window
 ])
 def test_shared_tiles_count_every_token_once(cuda_lib, B, hq, hkv, D, bs, lens, R, dtype, kv,
-                                             splits):
+                                             splits, window):
     case = tile_index_case(B, hq, hkv, D, bs, lens, R=R, dtype=dtype, kv_dtype=kv)
-    e = tile_index_expected(lens, R, hq, hkv, D)
+    e = tile_index_expected(lens, R, hq, hkv, D, window=window)
     for det in (False, True):
-        y = to_np(run(cuda_lib, case, splits=splits, deterministic=det))
+        y = to_np(run(cuda_lib, case, splits=splits, deterministic=det, window=window))
         err = np.abs(y - e).max() / np.abs(e).max()
         assert err <= 1e-2, f"deterministic={det}: error {err:.2e} (a tile is 16 / L)"
     no_device_errors(cuda_lib)

@@ -38,6 +38,9 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib):
     cases = [
         pi.make_case(1, 24, 4, 256, 784, [5000], seed=31, poison="kv_nan").to("cuda"),
         pi.make_case(3, 32, 8, 128, 16, [4097, 1000, 2222], seed=32, poison="v_nan").to("cuda"),
+        # long enough that the splits share the tail through the array's tile counters
+        pi.make_case(1, 8, 8, 128, 16, [32768], seed=34, poison="kv_nan", device="cuda"),
+        pi.make_case(1, 8, 8, 128, 16, [32000], seed=35, device="cuda"),
     ]
     for c in cases:
         S, _ = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.block_size, c.max_seq_len)
