@@ -204,9 +204,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   if (t_lo + split * p.P >= L) return;  // this split lies past the sequence: nothing to do
   const int n_splits = (L - t_lo + p.P - 1) / p.P;
   // Work sharing among the splits of one (sequence, KV head). Every split streams
-  // its static share; the tokens past the n static shares go out one 16-token tile
-  // at a time from a counter in the workspace, so that splits on faster SMs take
-  // more of them and all end together. The merge kernel resets the counter.
+  // its static share; the tokens past the n static shares go out one tile at a
+  // time from a counter in the workspace, so that splits on faster SMs take more of
+  // them and all end together. The merge kernel resets the counter.
   const bool steal = p.Ps < p.P && n_splits > 1;
   const int s_hi = steal ? min(L, s_lo + p.Ps) : min(L, t_lo + (split + 1) * p.P);
   const int n_stat = (s_hi - s_lo + C::TW - 1) / C::TW;  // static tiles of the CTA (>= 1)
