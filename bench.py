@@ -242,14 +242,14 @@ def load_peaks():
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
 # A capture holds only for the kernel sources it was taken on: when their SHA-256
 # differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "b3705c8c009660fbd32d0d7c9914796b0db83feba507db354d8288dc0f796253"
+TRAFFIC_SOURCES_SHA256 = "1e44bc786cd18f74cdc0082ddf77d9ff099bda513bbe833f135c95179410c5b5"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
-    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537048064 + 984661},
-    # 24q/4kv, block 784, batch 1, 32768 tokens: two launches
-    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134301056 + 3026944},
-    # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: two launches
-    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268604544 + 2941568},
+    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537067264 + 1034923},
+    # 24q/4kv, block 784, batch 1, 32768 tokens: three launches
+    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134299989 + 961536},
+    # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: three launches
+    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268610560 + 1094059},
 }
 
 

@@ -345,6 +345,44 @@ def test_all_empty_batch(cuda_lib):
     assert torch.all(out == 0)
 
 
+def test_million_token_context(cuda_lib):
+    # one KV head with 8 query heads over 2^20 - 3 tokens: hundreds of splits (more
+    # than the merge keeps in registers), a shared tail, a ragged last tile
+    L = (1 << 20) - 3
+    case = pi.make_case(1, 8, 1, 128, 16, [L], seed=23, poison="kv_nan", device="cuda")
+    S, P = cuda_lib.plan(1, 8, 1, 128, 16, L)
+    assert S > 64
+    y = run(cuda_lib, case)
+    assert torch.isfinite(y).all()
+    check_sampled(cuda_lib, case, y, [(0, 0)], "1M tokens")
+    no_device_errors(cuda_lib)
+
+
+def test_large_batch_of_short_sequences(cuda_lib):
+    # 1024 sequences x 8 KV heads: more (sequence, KV head) pairs than the shared-tile
+    # counters cover, lengths 0..200 including empty ones
+    rng = np.random.default_rng(24)
+    lens = [int(x) for x in rng.integers(0, 201, size=1024)]
+    case = pi.make_case(1024, 16, 8, 128, 16, lens, seed=24, poison="v_nan", device="cuda")
+    y = run(cuda_lib, case)
+    assert torch.isfinite(y).all()
+    pairs = sorted({(int(b), int(h)) for b, h in zip(rng.integers(0, 1024, 16), rng.integers(0, 8, 16))}
+                   | {(int(np.argmax(lens)), 7)})
+    check_sampled(cuda_lib, case, y, pairs, "large batch")
+    for b in np.nonzero(np.array(lens) == 0)[0][:4]:
+        assert torch.all(y[int(b)] == 0)
+    no_device_errors(cuda_lib)
+
+
+def test_block_size_one(cuda_lib):
+    # every token in its own block: one table entry per token
+    case = pi.make_case(2, 16, 4, 128, 1, [3001, 77], seed=25, poison="kv_nan")
+    assert_parity(to_np(run(cuda_lib, case)), oracle_case(case), what="block size 1")
+    case = pi.make_case(1, 24, 4, 256, 1, [1234], seed=26)
+    assert_parity(to_np(run(cuda_lib, case)), oracle_case(case), what="block size 1, D 256")
+    no_device_errors(cuda_lib)
+
+
 @pytest.mark.parametrize("hq,hkv,D,bs,dtype", [
     (5, 1, 128, 16, "bf16"), (7, 1, 256, 16, "f16"), (16, 1, 128, 32, "bf16"),
     (12, 1, 256, 784, "bf16"), (32, 2, 128, 16, "f16"), (3, 3, 256, 48, "bf16"),
