@@ -107,6 +107,11 @@ typedef void* pa_stream_t; /* cudaStream_t */
  *           on timing and repeated calls may differ in the last bit (each within
  *           the usual error). PA_FLAG_DETERMINISTIC keeps fixed splits: repeated
  *           calls give bitwise identical outputs. Other bits: PA_ERR_INVALID_ARG.
+ *   total_tokens  0, or the sum of seq_lens over the batch, known on the host like
+ *           max_seq_len. It lets the planner estimate how many context splits hold
+ *           tokens in a batch of mixed lengths; only the split plan depends on it
+ *           (a wrong value costs speed, not correctness). Negative, or above
+ *           B * max_seq_len: PA_ERR_INVALID_ARG. Ignored with a window.
  * All other fields mean what the pa_decode parameters of the same name mean.
  */
 typedef struct pa_decode_args {
@@ -126,6 +131,7 @@ typedef struct pa_decode_args {
   float k_scale, v_scale;
   int32_t q_len;
   uint32_t flags;
+  int64_t total_tokens;
 } pa_decode_args;
 
 #define PA_FLAG_DETERMINISTIC 1u

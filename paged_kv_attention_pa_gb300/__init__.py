@@ -63,7 +63,7 @@ class DecodeArgs(ctypes.Structure):
         ("scale", _c.c_float), ("dtype", _c.c_int32), ("splits", _c.c_int32),
         ("window", _c.c_int32), ("kv_dtype", _c.c_int32),
         ("k_scale", _c.c_float), ("v_scale", _c.c_float), ("q_len", _c.c_int32),
-        ("flags", _c.c_uint32),
+        ("flags", _c.c_uint32), ("total_tokens", _c.c_int64),
     ]
 
 
@@ -124,7 +124,7 @@ def _stream_handle(device: torch.device, stream) -> int:
 def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
               max_seq_len: Optional[int] = None, splits: int = 0, window: int = 0,
               k_scale: float = 1.0, v_scale: float = 1.0,
-              deterministic: bool = False) -> DecodeArgs:
+              deterministic: bool = False, total_tokens: int = 0) -> DecodeArgs:
     """Check shapes / dtypes / devices and fill a pa_decode_args. q is [B, Hq, D], or
     [B, R, Hq, D] for R causal query rows per sequence."""
     if q.dim() not in (3, 4) or k_cache.dim() != 4 or v_cache.dim() != 4:
@@ -171,6 +171,7 @@ def make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale: float,
     a.kv_dtype = PA_KV_FP8_E4M3 if fp8 else PA_KV_AS_DTYPE
     a.k_scale, a.v_scale = (float(k_scale), float(v_scale)) if fp8 else (1.0, 1.0)
     a.flags = PA_FLAG_DETERMINISTIC if deterministic else 0
+    a.total_tokens = int(total_tokens)
     return a
 
 
@@ -196,7 +197,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            out: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
            splits: int = 0, workspace: Optional[torch.Tensor] = None, stream=None,
            window: int = 0, k_scale: float = 1.0, v_scale: float = 1.0,
-           deterministic: bool = False) -> torch.Tensor:
+           deterministic: bool = False, total_tokens: int = 0) -> torch.Tensor:
     """out[b, h] = softmax(scale * q[b,h] . K_b^T) V_b over the paged context of sequence b.
 
     q [B, Hq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D]; block_tables
@@ -207,13 +208,15 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     stored value * k_scale / v_scale. deterministic=True keeps fixed context splits, so
     that repeated calls are bitwise identical (by default the splits of a long context
     share out its tail as they finish, and the last bit may vary from call to call).
-    Asynchronous on the current (or given) stream.
+    total_tokens, the sum of seq_lens when the caller knows it on the host, helps the
+    split plan for batches of mixed lengths. Asynchronous on the current (or given)
+    stream.
     """
     lib = load()
     if out is None:
         out = torch.empty_like(q)
     args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len, splits,
-                     window, k_scale, v_scale, deterministic)
+                     window, k_scale, v_scale, deterministic, total_tokens)
     _ensure_device(lib, q.device.index)
     sh = _stream_handle(q.device, stream)
     ws = workspace if workspace is not None else workspace_for(args, q.device, sh)
@@ -264,7 +267,7 @@ def decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out=None,
 
 def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
          splits: int = 0, sm_count: int = 0, window: int = 0,
-         kv_fp8: bool = False) -> Tuple[int, int]:
+         kv_fp8: bool = False, total_tokens: int = 0) -> Tuple[int, int]:
     """(splits, tokens per split) the library would launch with. sm_count <= 0 asks
     the current device; a positive sm_count needs no GPU. kv_fp8: FP8 E4M3 caches
     (their warp tile is 32 tokens, so splits are multiples of 32)."""
@@ -279,6 +282,7 @@ def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
     a.window = window
     if kv_fp8:
         a.kv_dtype, a.k_scale, a.v_scale = PA_KV_FP8_E4M3, 1.0, 1.0
+    a.total_tokens = int(total_tokens)
     S, P = ctypes.c_int(0), ctypes.c_int(0)
     rc = lib.pa_decode_plan(ctypes.byref(a), int(sm_count), ctypes.byref(S), ctypes.byref(P))
     if rc != PA_OK:

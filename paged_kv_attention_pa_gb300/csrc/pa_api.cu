@@ -24,7 +24,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // crosses from one split's tokens into the next). The unit of parallel work is a (sequence,
 // KV head, split) CTA, one resident per SM. The cost of a plan is the number of
 // CTA waves times the tokens a CTA streams plus its fixed cost; candidates are
-// one split and the largest split counts that fill exactly 1..4 waves.
+// one split, the largest split counts that fill exactly 1..4 waves, and 2..4
+// splits (which can shorten the last wave when there are more (sequence, KV head)
+// pairs than SMs).
 struct Plan {
   int S;
   int P;
@@ -46,7 +48,8 @@ bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, int64
 }
 
 bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_size,
-               int64_t max_len, int requested, int64_t quantum, Plan* out) {
+               int64_t max_len, int requested, int64_t quantum, int64_t total_tokens,
+               Plan* out) {
   if (max_len <= 0) {
     *out = {1, (int)quantum};
     return true;
@@ -58,13 +61,22 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
   if (requested > 0) return plan_for(requested, max_len, p_max, false, quantum, out);
   bool found = false;
   int64_t best_cost = 0;
-  const int64_t cands[6] = {1, sm / units, 2 * sm / units, 3 * sm / units, 4 * sm / units,
-                            ceil_div(sm, units)};
+  const int64_t cands[9] = {1, sm / units, 2 * sm / units, 3 * sm / units, 4 * sm / units,
+                            ceil_div(sm, units), 2, 3, 4};
+  // CTAs with tokens to stream: every split of every pair when the lengths are
+  // unknown (all taken as max_len); given the batch's total context tokens, the
+  // splits past each sequence's end are estimated away (a sequence's last split
+  // counted as half full on average).
+  auto live_ctas = [&](const Plan& pl) -> int64_t {
+    const int64_t all = units * pl.S;
+    if (total_tokens <= 0) return all;
+    return std::min(all, Hkv * (ceil_div(total_tokens, pl.P) + ceil_div(B, 2)));
+  };
   for (int64_t c : cands) {
     if (c < 1) continue;
     Plan pl{};
     if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
-    const int64_t waves = ceil_div(units * pl.S, sm);
+    const int64_t waves = ceil_div(live_ctas(pl), sm);
     const int64_t overhead_tokens = pa::kSplitOverheadBytes / (4 * D);  // K + V bytes per token
     const int64_t cost = waves * (pl.P + overhead_tokens);
     if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
@@ -138,6 +150,7 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   }
   if (a->kv_dtype != PA_KV_AS_DTYPE && a->kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
   if (a->flags & ~PA_FLAG_DETERMINISTIC) return PA_ERR_INVALID_ARG;
+  if (a->total_tokens < 0) return PA_ERR_INVALID_ARG;
   if (a->kv_dtype == PA_KV_FP8_E4M3 &&
       !(a->k_scale > 0.f && a->v_scale > 0.f && a->k_scale < INFINITY && a->v_scale < INFINITY))
     return PA_ERR_INVALID_ARG;
@@ -148,6 +161,7 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   int64_t ml = a->max_seq_len <= 0 ? cap : a->max_seq_len;
   if (ml > cap) return PA_ERR_OUT_OF_RANGE;
   if (ml > INT_MAX) return PA_ERR_OUT_OF_RANGE;
+  if (a->total_tokens > (int64_t)a->B * ml) return PA_ERR_INVALID_ARG;  // contradicts max_seq_len
   *max_len = ml;
   return PA_OK;
 }
@@ -156,6 +170,10 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
 int64_t tile_tokens(const pa_decode_args* a) {
   return pa::tile_tokens(a->D, a->kv_dtype == PA_KV_FP8_E4M3);
 }
+
+// The batch's total context tokens for the planner (0: unknown). A window bounds
+// each sequence's tokens in a way the total does not tell, so it is not used then.
+int64_t plan_tokens(const pa_decode_args* a) { return a->window > 0 ? 0 : a->total_tokens; }
 
 // Tokens one sequence's splits must cover: a sliding window bounds them.
 int64_t plan_len(const pa_decode_args* a, int64_t max_len) {
@@ -200,7 +218,7 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
   if (sm_count <= 0) return PA_ERR_CUDA;
   Plan plan{};
   if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
-                 tile_tokens(a), &plan))
+                 tile_tokens(a), plan_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   *splits = plan.S;
   *partition_tokens = plan.P;
@@ -270,7 +288,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   if (sm <= 0) return PA_ERR_CUDA;
   Plan plan{};
   if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
-                 tile_tokens(a), &plan))
+                 tile_tokens(a), plan_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const int rows = a->q_len > 0 ? a->q_len : 1;
