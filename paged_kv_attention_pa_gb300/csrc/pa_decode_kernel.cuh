@@ -83,7 +83,6 @@ struct Cfg {
   static constexpr int SMEM = RING + FIXED;
   static_assert((TW * CPR) % 32 == 0, "tile shape");
   static_assert(DEPTH >= 2, "need at least two slots per warp");
-  static_assert(NW * GT * (D + 6) * 4 <= RING, "CTA merge must fit");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
@@ -530,51 +529,42 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) l[nt][h] += __shfl_xor_sync(0xffffffffu, l[nt][h], o2);
 
-  // ---- merge the warps (the ring is free: every copy has landed and been consumed).
-  // Each warp first rescales its state to the CTA-wide maximum of every column, so
-  // that the final pass only sums: it reads 8 consecutive d of one column per item
-  // as two 16-byte words per warp and writes them with one 16-byte store.
-  // Accumulator rows are padded by 4 floats, so that the fragment writes (columns
-  // 2 tig + {0, 1}, rows gid) fall in distinct banks.
+  // ---- merge the warps. Each warp writes its state (m, l, unscaled accumulators)
+  // into its own ring, which only it has used: every one of its copies has landed
+  // and been consumed. After one barrier, the final pass reads all warps' states
+  // and weighs each by 2^(m_w - M) with M the CTA maximum of the column: it sums
+  // 8 consecutive d of one column per item as two 16-byte words per warp and
+  // writes them with one 16-byte store. Accumulator rows are padded by 4 floats,
+  // so that the fragment writes (columns 2 tig + {0, 1}, rows gid) fall in
+  // distinct banks.
   constexpr int AP = D + 4;
-  __syncthreads();
-  float* mw = reinterpret_cast<float*>(ring);  // [NW][GT] running maxima
-  float* lw = mw + kWarps * GT;                // [NW][GT] rescaled denominators
-  float* aw = lw + kWarps * GT;                // [NW][GT][AP] rescaled accumulators
-  if (gid == 0) {
+  constexpr int WSTATE = GT * (AP + 2);  // floats of one warp's state
+  static_assert(WSTATE * 4 <= C::DEPTH * C::SLOT_BYTES, "a warp's state fits in its ring");
+  auto wstate = [&](int w) { return reinterpret_cast<float*>(ring + w * C::DEPTH * C::SLOT_BYTES); };
+  {
+    float* mw = wstate(warp);  // [GT] running maxima, [GT] sums, [GT][AP] accumulators
+    float* lw = mw + GT;
+    float* aw = lw + GT;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mw[warp * GT + nt * 8 + 2 * tig] = m[nt][0];
-      mw[warp * GT + nt * 8 + 2 * tig + 1] = m[nt][1];
-    }
-  }
-  __syncthreads();
+      const int c0 = nt * 8 + 2 * tig;
+      if (gid == 0) {
+        mw[c0] = m[nt][0];
+        mw[c0 + 1] = m[nt][1];
+        lw[c0] = l[nt][0];
+        lw[c0 + 1] = l[nt][1];
+      }
+      float* a0 = aw + c0 * AP;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int c0 = nt * 8 + 2 * tig;
-    float f[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GT + c0 + h]);
-      // a warp that saw no token of the column (m = -inf) contributes nothing
-      f[h] = m[nt][h] == -INFINITY ? 0.f : exp2f(m[nt][h] - M);
-    }
-    if (gid == 0) {
-      lw[warp * GT + c0] = l[nt][0] * f[0];
-      lw[warp * GT + c0 + 1] = l[nt][1] * f[1];
-    }
-    float* a0 = aw + (warp * GT + c0) * AP;
-#pragma unroll
-    for (int dd = 0; dd < C::KS; ++dd) {
-      // rows gid and gid + 8 of d-block dd (permuted for fp8 caches, see the PV step)
-      const int dlo = F8 ? 2 * C::KS * gid + 2 * dd : dd * 16 + gid;
-      const int dhi = F8 ? dlo + 1 : dlo + 8;
-      a0[dlo] = o[nt][dd][0] * f[0];
-      a0[AP + dlo] = o[nt][dd][1] * f[1];
-      a0[dhi] = o[nt][dd][2] * f[0];
-      a0[AP + dhi] = o[nt][dd][3] * f[1];
+      for (int dd = 0; dd < C::KS; ++dd) {
+        // rows gid and gid + 8 of d-block dd (permuted for fp8 caches, see the PV step)
+        const int dlo = F8 ? 2 * C::KS * gid + 2 * dd : dd * 16 + gid;
+        const int dhi = F8 ? dlo + 1 : dlo + 8;
+        a0[dlo] = o[nt][dd][0];
+        a0[AP + dlo] = o[nt][dd][1];
+        a0[dhi] = o[nt][dd][2];
+        a0[AP + dhi] = o[nt][dd][3];
+      }
     }
   }
   __syncthreads();
@@ -584,16 +574,22 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   constexpr int DV = D / 8;  // items per column
   for (int it = threadIdx.x; it < cols * DV; it += kThreads) {
     const int g = it / DV, d0 = (it % DV) * 8;  // g: column
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wstate(w)[g]);
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float den = 0.f, M = -INFINITY;
+    float den = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float4* src = reinterpret_cast<const float4*>(aw + (w * GT + g) * AP + d0);
+      const float* st = wstate(w);
+      const float mwg = st[g];
+      // a warp that saw no token of the column (m = -inf) contributes nothing
+      const float f = mwg == -INFINITY ? 0.f : exp2f(mwg - M);
+      const float4* src = reinterpret_cast<const float4*>(st + 2 * GT + g * AP + d0);
       const float4 x = src[0], y = src[1];
-      v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
-      v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
-      den += lw[w * GT + g];
-      M = fmaxf(M, mw[w * GT + g]);
+      v[0] += f * x.x; v[1] += f * x.y; v[2] += f * x.z; v[3] += f * x.w;
+      v[4] += f * y.x; v[5] += f * y.y; v[6] += f * y.z; v[7] += f * y.w;
+      den += f * st[GT + g];
     }
     // cache values are stored values times v_scale (1 unless fp8); a column whose
     // row sees no token of this split has M = -inf and den = 0
