@@ -33,6 +33,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -243,14 +244,14 @@ def load_peaks():
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
 # A capture holds only for the kernel sources it was taken on: when their SHA-256
 # differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "eae8cf4d15874f86d4ccb0f17ef285d456596fcb593faee034a905b426c4aefc"
+TRAFFIC_SOURCES_SHA256 = "3d64b2ffb3c7c761ed75071daa6258d1b55a6a282199ddf0f8da53296bc6cffa"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
-    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537067264 + 1034923},
+    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537048661 + 988501},
     # 24q/4kv, block 784, batch 1, 32768 tokens: three launches
-    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134299989 + 961536},
+    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134299819 + 904107},
     # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: three launches
-    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268610560 + 1094059},
+    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268604416 + 958549},
 }
 
 
@@ -582,6 +583,24 @@ def run_ours(args, rank, world, local_rank):
             del c.insts[1:]
             torch.cuda.empty_cache()
 
+    # µs/call against context at batch 1 with 4 KV heads (the hybrid layer): least
+    # squares over 4K-32K tokens, with its R^2
+    linearity = None
+    pts = []
+    for c in curve:
+        m = re.match(r"hybrid L=(\d+)$", c["cell"])
+        if m and int(m.group(1)) >= 4096:
+            pts.append((int(m.group(1)), c["us_per_call"]))
+    if len(pts) >= 3:
+        x = np.array([p[0] / 1024.0 for p in pts])
+        y = np.array([p[1] for p in pts])
+        A = np.vstack([x, np.ones_like(x)]).T
+        (slope, icpt), *_ = np.linalg.lstsq(A, y, rcond=None)
+        r2 = 1.0 - float(((y - A @ np.array([slope, icpt])) ** 2).sum() / ((y - y.mean()) ** 2).sum())
+        linearity = {"range_tokens": [int(min(p[0] for p in pts)), int(max(p[0] for p in pts))],
+                     "slope_us_per_1k_tokens": round(float(slope), 4),
+                     "intercept_us": round(float(icpt), 3), "r2": round(r2, 5)}
+
     budget = float(os.environ.get("PA_BENCH_CPU_BUDGET_S", "12"))
     cb_bytes, cb_s, cb_desc = oracle_sample(budget, device=dev)
     achieved = alg / (ms_step_max * 1e-3) / 1e9
@@ -626,6 +645,8 @@ def run_ours(args, rank, world, local_rank):
                                 round(max(step_ms), 4)],
         "curve": curve,
     }
+    if linearity:
+        line["linearity"] = linearity
     print(json.dumps(line), flush=True)
 
 
