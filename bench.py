@@ -20,7 +20,7 @@ four times the L2) that every call reads HBM, as an engine replays its layers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload grid|hybrid|mixed|first|cell|window|rows]
-                    [--cell Hq,Hkv,B,L,D,bs]
+                    [--cell Hq,Hkv,B,L,D,bs] [--kv-dtype bf16|fp8] [--no-curve]
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (there is no other implementation to run). With torchrun (N > 1) every
@@ -282,6 +282,27 @@ def traffic_per_call(alg_bytes_per_call: float, D: int, kv: str):
     return round(alg_bytes_per_call * ratio), (
         f"ncu dram bytes / algorithmic bytes = {ratio:.5f} on a head_dim {D} {kv} cell, "
         "scaled by the call's KV bytes")
+
+
+def hybrid_linearity(curve, min_tokens=4096):
+    """Least-squares fit of µs/call against context for the hybrid layer's cells
+    (batch 1, 4 KV heads) of at least min_tokens, with its R^2; None without 3 points."""
+    pts = []
+    for c in curve:
+        m = re.match(r"hybrid L=(\d+)$", c["cell"])
+        if m and int(m.group(1)) >= min_tokens:
+            pts.append((int(m.group(1)), float(c["us_per_call"])))
+    if len(pts) < 3:
+        return None
+    x = np.array([p[0] / 1024.0 for p in pts])
+    y = np.array([p[1] for p in pts])
+    A = np.vstack([x, np.ones_like(x)]).T
+    (slope, icpt), *_ = np.linalg.lstsq(A, y, rcond=None)
+    ss_tot = float(((y - y.mean()) ** 2).sum())
+    r2 = 1.0 - float(((y - A @ np.array([slope, icpt])) ** 2).sum()) / ss_tot if ss_tot > 0 else 1.0
+    return {"range_tokens": [min(p[0] for p in pts), max(p[0] for p in pts)],
+            "slope_us_per_1k_tokens": round(float(slope), 4),
+            "intercept_us": round(float(icpt), 3), "r2": round(r2, 5)}
 
 
 class ClockSampler:
@@ -583,23 +604,7 @@ def run_ours(args, rank, world, local_rank):
             del c.insts[1:]
             torch.cuda.empty_cache()
 
-    # µs/call against context at batch 1 with 4 KV heads (the hybrid layer): least
-    # squares over 4K-32K tokens, with its R^2
-    linearity = None
-    pts = []
-    for c in curve:
-        m = re.match(r"hybrid L=(\d+)$", c["cell"])
-        if m and int(m.group(1)) >= 4096:
-            pts.append((int(m.group(1)), c["us_per_call"]))
-    if len(pts) >= 3:
-        x = np.array([p[0] / 1024.0 for p in pts])
-        y = np.array([p[1] for p in pts])
-        A = np.vstack([x, np.ones_like(x)]).T
-        (slope, icpt), *_ = np.linalg.lstsq(A, y, rcond=None)
-        r2 = 1.0 - float(((y - A @ np.array([slope, icpt])) ** 2).sum() / ((y - y.mean()) ** 2).sum())
-        linearity = {"range_tokens": [int(min(p[0] for p in pts)), int(max(p[0] for p in pts))],
-                     "slope_us_per_1k_tokens": round(float(slope), 4),
-                     "intercept_us": round(float(icpt), 3), "r2": round(r2, 5)}
+    linearity = hybrid_linearity(curve)
 
     budget = float(os.environ.get("PA_BENCH_CPU_BUDGET_S", "12"))
     cb_bytes, cb_s, cb_desc = oracle_sample(budget, device=dev)

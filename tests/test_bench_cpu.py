@@ -1,0 +1,41 @@
+"""Host-side helpers of bench.py (CPU only): the µs/call-vs-context fit and the
+DRAM-traffic figure scaled from ncu captures."""
+import bench
+
+
+def test_linearity_fit_recovers_a_line():
+    curve = [{"cell": f"hybrid L={L}", "us_per_call": 5.0 + 0.5 * L / 1024} for L in
+             (500, 1024, 2048, 4096, 8192, 16384, 32768)]
+    fit = bench.hybrid_linearity(curve)
+    assert fit["range_tokens"] == [4096, 32768]      # only contexts >= 4K
+    assert abs(fit["slope_us_per_1k_tokens"] - 0.5) < 1e-9
+    assert abs(fit["intercept_us"] - 5.0) < 1e-9
+    assert fit["r2"] == 1.0
+
+
+def test_linearity_fit_needs_three_points_and_sees_curvature():
+    assert bench.hybrid_linearity([{"cell": "hybrid L=4096", "us_per_call": 1.0}]) is None
+    assert bench.hybrid_linearity([{"cell": "8/8 B=1 L=4096", "us_per_call": 1.0}] * 5) is None
+    curve = [{"cell": f"hybrid L={L}", "us_per_call": (L / 1024) ** 2} for L in
+             (4096, 8192, 16384, 32768)]
+    assert bench.hybrid_linearity(curve)["r2"] < 0.99
+
+
+def test_traffic_scaled_from_the_matching_capture(monkeypatch):
+    monkeypatch.setattr(bench, "TRAFFIC_SOURCES_SHA256", bench.kernel_sources_sha256())
+    cap = bench.TRAFFIC_CAPTURES[(128, "bf16")]
+    t, note = bench.traffic_per_call(cap["alg_bytes"], 128, "bf16")
+    assert t == cap["dram_bytes"]
+    assert "head_dim 128 bf16" in note
+    assert bench.traffic_per_call(1e9, 64, "bf16")[0] is None   # no capture for the layout
+
+
+def test_traffic_is_null_once_the_device_code_changes(monkeypatch):
+    monkeypatch.setattr(bench, "TRAFFIC_SOURCES_SHA256", "0" * 64)
+    t, note = bench.traffic_per_call(1e9, 128, "bf16")
+    assert t is None and "changed" in note
+
+
+def test_captures_read_each_kv_byte_about_once():
+    for (D, kv), cap in bench.TRAFFIC_CAPTURES.items():
+        assert 1.0 <= cap["dram_bytes"] / cap["alg_bytes"] < 1.02, (D, kv)
