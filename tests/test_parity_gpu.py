@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import pa_inputs as pi
-from harness import assert_parity, oracle_case, oracle_rows, oracle_rows_case, read_golden
+from harness import (REL_LINF_TOL, assert_parity, oracle_case, oracle_rows, oracle_rows_case,
+                     read_golden)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,10 +49,15 @@ def rel_diff(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
-# Two outputs of one call that differ only in the order of the fp32 sums (the splits
-# of a long context share out its tail tile by tile) differ by rounding of the
-# output type: at most about one bf16 step (2^-8 relative) on the max-abs scale.
-ORDER_TOL = 4e-3
+# Two outputs of one call whose splits group the tokens differently (the splits of a
+# long context share out its tail tile by tile) differ by more than fp32 summation
+# order: each warp rounds its softmax weights to the MMA type relative to its own
+# running maximum, which depends on the tokens it streamed. That is the rounding the
+# error band of "vLLM's custom ROCm paged-attention kernel wins all sixty cells"
+# (§3) already contains, so two such outputs are held to the parity bar of each
+# other; each is also checked against the oracle, and the exact tile-count test
+# catches a token counted twice or skipped.
+ORDER_TOL = REL_LINF_TOL
 
 
 def check_sampled(pa, case, out, pairs, what):
@@ -425,6 +431,54 @@ def test_cuda_graph_replay(cuda_lib):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+def test_graph_replays_rearm_the_tile_counters(cuda_lib):
+    # a call whose splits share their tail, captured once and replayed: every replay
+    # must find the counters at zero again (the merge grid rearms them)
+    case = pi.make_case(1, 8, 8, 128, 16, [32768], seed=27, device="cuda")
+    ref = run(cuda_lib, case, deterministic=True)
+    check_sampled(cuda_lib, case, ref, [(0, 0), (0, 7)], "graph reference")
+    out = torch.empty_like(case.q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        kw = dict(out=out, max_seq_len=case.max_seq_len)
+        cuda_lib.decode(case.q, case.k_cache, case.v_cache, case.block_tables, case.seq_lens,
+                        case.scale, **kw)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                cuda_lib.decode(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                case.seq_lens, case.scale, **kw)
+    for _ in range(5):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert rel_diff(out, ref) <= ORDER_TOL
+    no_device_errors(cuda_lib)
+
+
+def test_two_streams_with_their_own_workspaces(cuda_lib):
+    # sharing calls in flight on two streams at once, each with the binding's default
+    # workspace of its stream (its own tile counters)
+    cases = [pi.make_case(1, 8, 8, 128, 16, [32768 - 97 * i], seed=28 + i, device="cuda")
+             for i in range(2)]
+    refs = [run(cuda_lib, c, deterministic=True) for c in cases]
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [torch.empty_like(c.q) for c in cases]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for c, o, st in zip(cases, outs, streams):
+            with torch.cuda.stream(st):
+                cuda_lib.decode(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
+                                out=o, max_seq_len=c.max_seq_len, stream=st)
+    torch.cuda.synchronize()
+    for o, r in zip(outs, refs):
+        assert rel_diff(o, r) <= ORDER_TOL
+    for st in streams:
+        ws = cuda_lib.default_workspace(cases[0].q.device, st)
+        assert ws is not None and cuda_lib.read_device_errors(ws, stream=st) == 0
 
 
 # ------------------------------------------------------------------ sliding window
