@@ -32,6 +32,15 @@ struct Plan {
   int P;
 };
 
+// A CTA's fixed cost (launch, first round trip, epilogue) expressed as the KV bytes
+// it could have streamed meanwhile; the cost model charges it once per CTA and wave.
+// Swept on GB300 (128 KiB .. 1 MiB): 256 KiB gave the best GQA grid and mixed batch,
+// and the fewest wrong picks against ~60 forced-split timings (B = 1..64).
+#ifndef PA_SPLIT_OVERHEAD_BYTES
+#define PA_SPLIT_OVERHEAD_BYTES (256 << 10)
+#endif
+constexpr int64_t kSplitOverheadBytes = PA_SPLIT_OVERHEAD_BYTES;
+
 bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, int64_t quantum,
               Plan* out) {
   int64_t P = round_up(ceil_div(max_len, std::max<int64_t>(S_req, 1)), quantum);
@@ -77,7 +86,7 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
     Plan pl{};
     if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
     const int64_t waves = ceil_div(live_ctas(pl), sm);
-    const int64_t overhead_tokens = pa::kSplitOverheadBytes / (4 * D);  // K + V bytes per token
+    const int64_t overhead_tokens = kSplitOverheadBytes / (4 * D);  // K + V bytes per token
     const int64_t cost = waves * (pl.P + overhead_tokens);
     if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
       *out = pl;

@@ -34,9 +34,6 @@ constexpr int tile_tokens(int D, bool fp8) {
   return fp8 ? (D == 128 ? PA_TILE_TOKENS_F8_D128 : PA_TILE_TOKENS_F8_D256)
              : (D == 128 ? PA_TILE_TOKENS_D128 : PA_TILE_TOKENS_D256);
 }
-#ifndef PA_SPLIT_OVERHEAD_BYTES
-#define PA_SPLIT_OVERHEAD_BYTES (1 << 20)
-#endif
 // Work sharing among the splits of a sequence: each split keeps about
 // (1 - 1/kStealDiv) of its P tokens as a static share, and the rest of the context
 // is claimed tile by tile through one counter per (sequence, KV head) held in the
@@ -55,9 +52,6 @@ constexpr int kStealUnits = 2048;
 constexpr int kHeaderBytes = 256 + kStealUnits * 4;  // error word, then the counters
 static_assert(kHeaderBytes % 256 == 0, "header keeps 256-byte alignment");
 static_assert(kHeaderBytes == PA_WORKSPACE_HEADER_BYTES, "header size is part of the ABI");
-// A CTA's fixed cost (launch, first round trip, epilogue) expressed as the KV bytes
-// it could have streamed meanwhile; the split planner charges it once per CTA.
-constexpr int kSplitOverheadBytes = PA_SPLIT_OVERHEAD_BYTES;
 
 struct DecodeParams {
   const void* q;

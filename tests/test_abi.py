@@ -169,11 +169,24 @@ def test_forced_splits():
     assert P == 32 and S == 33
 
 
-def test_large_batch_needs_no_split():
-    S, P = pa.plan(64, 32, 8, 128, 16, 8192, sm_count=SM)
-    assert S == 1 and P >= 8192
-    S, P = pa.plan(64, 32, 8, 128, 16, 4096, sm_count=SM)
-    assert S == 1
+def test_large_batch_plans():
+    # 512 (sequence, KV head) pairs on 152 SMs: one or two splits, never more
+    # (GB300, us per call for S = 1 / 2 / 3: 8K 343.8 / 338.8 / 362.9, 16K 678.8 /
+    # 637.9 / 678.0; at 4K one split is 4% faster than the two the model picks)
+    for L in (4096, 8192, 16384):
+        S, P = pa.plan(64, 32, 8, 128, 16, L, sm_count=SM)
+        assert S in (1, 2) and S * P >= L
+    assert pa.plan(64, 32, 8, 128, 16, 16384, sm_count=SM)[0] == 2
+    # 1024 pairs of short contexts: one split
+    assert pa.plan(128, 32, 8, 128, 16, 2048, sm_count=SM)[0] == 1
+
+
+def test_batch8_long_contexts_fill_three_waves():
+    # 64 pairs: three full waves of seven splits beat one wave of two at 16K-32K
+    # (GB300: 87.5 vs 93.0 us at 16K, 163.6 vs 174.0 us at 32K)
+    for L in (16384, 32768):
+        assert pa.plan(8, 32, 8, 128, 16, L, sm_count=SM)[0] == 7
+    assert pa.plan(8, 8, 8, 128, 16, 4096, sm_count=SM)[0] == 2  # 27.2 us, the best
 
 
 def test_total_tokens_hint():
@@ -182,7 +195,7 @@ def test_total_tokens_hint():
     # (GB300, forced splits: 752 / 715 / 709 / 692 us per call for 1 / 2 / 3 / 4)
     S0, _ = pa.plan(64, 32, 8, 128, 16, 32704, sm_count=SM)
     S1, P1 = pa.plan(64, 32, 8, 128, 16, 32704, sm_count=SM, total_tokens=64 * 16900)
-    assert S0 == 2 and S1 == 3 and S1 * P1 >= 32704
+    assert S0 == 2 and S1 == 4 and S1 * P1 >= 32704
     # a uniform batch's total gives the plan of no hint
     for B, Hkv, L in [(64, 8, 32768), (8, 8, 4096), (1, 4, 32768), (24, 8, 8192)]:
         assert pa.plan(B, 4 * Hkv, Hkv, 128, 16, L, sm_count=SM, total_tokens=B * L) == \
