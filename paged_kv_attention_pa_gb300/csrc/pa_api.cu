@@ -56,7 +56,7 @@ bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, int64
   return true;
 }
 
-bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_size,
+bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t kv_elem_bytes,
                int64_t max_len, int requested, int64_t quantum, int64_t total_tokens,
                Plan* out) {
   if (max_len <= 0) {
@@ -65,7 +65,6 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
   }
   const int64_t units = B * Hkv;
   const int64_t sm = sm_count > 0 ? sm_count : 1;
-  (void)block_size;
   const int64_t p_max = round_up(max_len, quantum);
   if (requested > 0) return plan_for(requested, max_len, p_max, false, quantum, out);
   bool found = false;
@@ -86,7 +85,8 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t block_si
     Plan pl{};
     if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
     const int64_t waves = ceil_div(live_ctas(pl), sm);
-    const int64_t overhead_tokens = kSplitOverheadBytes / (4 * D);  // K + V bytes per token
+    // the fixed cost in tokens of this cache: K + V bytes per token per KV head
+    const int64_t overhead_tokens = kSplitOverheadBytes / (2 * D * kv_elem_bytes);
     const int64_t cost = waves * (pl.P + overhead_tokens);
     if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
       *out = pl;
@@ -175,6 +175,9 @@ pa_status check_sizes(const pa_decode_args* a, int64_t* max_len) {
   return PA_OK;
 }
 
+// Bytes of one cache element.
+int64_t kv_elem_bytes(const pa_decode_args* a) { return a->kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2; }
+
 // Tokens per warp tile of the kernel that serves these arguments.
 int64_t tile_tokens(const pa_decode_args* a) {
   return pa::tile_tokens(a->D, a->kv_dtype == PA_KV_FP8_E4M3);
@@ -226,7 +229,7 @@ pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
   if (sm_count <= 0) sm_count = current_sm_count();
   if (sm_count <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm_count, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
+  if (!make_plan(sm_count, a->B, a->Hkv, a->D, kv_elem_bytes(a), plan_len(a, max_len), a->splits,
                  tile_tokens(a), plan_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   *splits = plan.S;
@@ -296,7 +299,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const int sm = current_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   Plan plan{};
-  if (!make_plan(sm, a->B, a->Hkv, a->D, a->block_size, plan_len(a, max_len), a->splits,
+  if (!make_plan(sm, a->B, a->Hkv, a->D, kv_elem_bytes(a), plan_len(a, max_len), a->splits,
                  tile_tokens(a), plan_tokens(a), &plan))
     return PA_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
