@@ -624,12 +624,30 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 // four split lanes.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
-  pdl_wait();  // the partials of the decode grid are complete and visible
-  pdl_launch_dependents();
+  constexpr int kPre = 16, kReg = 2;  // 4 * kPre == 32 * kReg
   __shared__ float part[4][64];
   const int b = blockIdx.z, row = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
   const int G = p.G, kvh = h / G, g = h - kvh * G;
   const int cols = G * p.q_len, c = row * G + g;  // the partials' column of (row, head)
+  const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int dl = tid & 63, sl = tid >> 6;
+  const int d = blockIdx.x * 64 + dl;
+  const float* acc = p.ws_acc + (base * cols + c) * D + d;
+  const float* pm = p.ws_m + base * cols + c;
+  const float* pl = p.ws_l + base * cols + c;
+  // This grid starts while the decode grid finishes. Before waiting for it, ask for
+  // the lines (and address translations) of this CTA's partials in L2, where the
+  // decode grid writes them: a prefetch returns nothing, so it cannot read stale data.
+  if (lane == 0)
+    for (int i = 0; i < kPre; ++i)
+      if (sl + 4 * i < p.S) prefetch_l2(acc + (size_t)(sl + 4 * i) * cols * D);
+  if (tid < 32 * kReg && tid < p.S) {
+    prefetch_l2(pm + (size_t)tid * cols);
+    prefetch_l2(pl + (size_t)tid * cols);
+  }
+  pdl_wait();  // the partials of the decode grid are complete and visible
+  pdl_launch_dependents();
   int L = __ldg(p.seq_lens + b);
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
   L = L < 0 ? 0 : (L > cap ? cap : L);
@@ -639,17 +657,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   // the decode grid is done with this (sequence, KV head)'s tile counter: rearm it
   if (p.Ps < p.P && blockIdx.x == 0 && row == 0 && g == 0 && threadIdx.x == 0)
     p.steal[(size_t)b * p.Hkv + kvh] = 0;
-  const size_t base = ((size_t)b * p.Hkv + kvh) * p.S;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int dl = tid & 63, sl = tid >> 6;
-  const int d = blockIdx.x * 64 + dl;
-  const float* acc = p.ws_acc + (base * cols + c) * D + d;
-  const float* pm = p.ws_m + base * cols + c;
-  const float* pl = p.ws_l + base * cols + c;
 
   // One round trip: this thread's accumulators of splits sl + 4 i (i < 16) and the
   // warp's maxima and sums of splits lane and lane + 32.
-  constexpr int kPre = 16, kReg = 2;  // 4 * kPre == 32 * kReg
   float av[kPre];
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {

@@ -35,6 +35,11 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
   return y;
 }
 
+// Ask for the L2 line holding p (no data returned; a hint the memory system may drop).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte shared-memory load from a shared-window address.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
