@@ -188,8 +188,10 @@ pa_status pa_decode_ex(const pa_decode_args* args, void* workspace, size_t works
 
 /*
  * The launch plan pa_decode_ex would use on a GPU with `sm_count` SMs: the number
- * of context splits and the tokens per split (a multiple of 16). Pure host
- * arithmetic; needs no GPU. sm_count <= 0 means the current device's SM count.
+ * of context splits and the tokens per split, a whole number of warp tiles (32
+ * tokens at head_dim 128 and for fp8 caches, 16 at head_dim 256). It depends on the
+ * sizes, max_seq_len, window, kv_dtype, splits and total_tokens of `args`. Pure
+ * host arithmetic; needs no GPU. sm_count <= 0 means the current device's SM count.
  */
 pa_status pa_decode_plan(const pa_decode_args* args, int sm_count, int* splits,
                          int* partition_tokens);
