@@ -89,7 +89,8 @@ typedef void* pa_stream_t; /* cudaStream_t */
  *   kv_dtype  PA_KV_AS_DTYPE (default) or PA_KV_FP8_E4M3: the caches hold one byte
  *           per element, [num_blocks, block_size, Hkv, D] as before; q and out keep
  *           `dtype`. fp8 K/V are widened exactly to fp16 for the tensor-core
- *           products (the queries are rounded to fp16, P is kept in fp16) with fp32
+ *           products (the queries are rounded to fp16, so bf16 query elements must
+ *           lie within fp16's range, |x| <= 65504; P is kept in fp16) with fp32
  *           accumulation. The pages list an fp8 cache as untested ("vLLM's custom
  *           ROCm paged-attention kernel wins all sixty cells", section 6).
  *   k_scale, v_scale  per-tensor dequantisation scales (finite, > 0) for an fp8
