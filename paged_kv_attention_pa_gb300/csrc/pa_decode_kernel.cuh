@@ -127,9 +127,13 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   };
 
   // Inputs may come from the previous kernel in the stream: wait for it (a no-op
-  // without a programmatic launch), then let the merge grid get scheduled.
+  // without a programmatic launch). A split grid then lets its merge grid get
+  // scheduled at once (small CTAs that prefetch the partials meanwhile); a grid
+  // that writes the output itself lets the next kernel launch only once its CTAs
+  // have streamed their tiles: the next call's CTAs, resident early on the SMs
+  // this grid leaves idle, measured slower than a later launch.
   pdl_wait();
-  pdl_launch_dependents();
+  if (p.S > 1) pdl_launch_dependents();
 
   // ---- prologue: everything the first copies depend on is requested at once (one
   // round trip): the context length, the query fragments and, speculatively, the
@@ -420,36 +424,61 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     // each column's limit (seq_len, and the causal limit of the column's query row);
     // rows past seq_len were never loaded
     uint32_t pb[MT][NT][2];
+    float x[NT][MT][4];
+    float mx[NT][2];
+    bool grow = false;  // some column of this lane sees a score above its running max
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float x[MT][4];
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      mx[nt][0] = mx[nt][1] = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int tok0 = t0 + 16 * mt + gid, tok1 = tok0 + 8;
-        x[mt][0] = tok0 < lim[nt][0] ? (s[mt][nt][0] + s2[mt][nt][0]) * sl2 : -INFINITY;
-        x[mt][1] = tok0 < lim[nt][1] ? (s[mt][nt][1] + s2[mt][nt][1]) * sl2 : -INFINITY;
-        x[mt][2] = tok1 < lim[nt][0] ? (s[mt][nt][2] + s2[mt][nt][2]) * sl2 : -INFINITY;
-        x[mt][3] = tok1 < lim[nt][1] ? (s[mt][nt][3] + s2[mt][nt][3]) * sl2 : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(x[mt][0], x[mt][2]));
-        mx1 = fmaxf(mx1, fmaxf(x[mt][1], x[mt][3]));
+        x[nt][mt][0] = tok0 < lim[nt][0] ? (s[mt][nt][0] + s2[mt][nt][0]) * sl2 : -INFINITY;
+        x[nt][mt][1] = tok0 < lim[nt][1] ? (s[mt][nt][1] + s2[mt][nt][1]) * sl2 : -INFINITY;
+        x[nt][mt][2] = tok1 < lim[nt][0] ? (s[mt][nt][2] + s2[mt][nt][2]) * sl2 : -INFINITY;
+        x[nt][mt][3] = tok1 < lim[nt][1] ? (s[mt][nt][3] + s2[mt][nt][3]) * sl2 : -INFINITY;
+        mx[nt][0] = fmaxf(mx[nt][0], fmaxf(x[nt][mt][0], x[nt][mt][2]));
+        mx[nt][1] = fmaxf(mx[nt][1], fmaxf(x[nt][mt][1], x[nt][mt][3]));
       }
-      // tile max per head over its tokens (lanes sharing tig)
+      grow = grow || mx[nt][0] > m[nt][0] || mx[nt][1] > m[nt][1];
+    }
+    // Most tiles raise no running max (all scale factors are exactly 1): they skip
+    // the cross-lane maxima and the rescaling, with bit-identical results. At
+    // head_dim 256, and with more than 8 columns, the skip measured slower per call:
+    // every tile rescales there.
+    const bool rescale = D != 128 || NT > 1 || __any_sync(0xffffffffu, grow);
 #pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+    for (int nt = 0; nt < NT; ++nt) {
+      float al0 = 1.f, al1 = 1.f;
+      if (rescale) {
+        float mx0 = mx[nt][0], mx1 = mx[nt][1];
+        // tile max per head over its tokens (lanes sharing tig)
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        }
+        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+        const float q0 = mn0 == -INFINITY ? 0.f : mn0, q1 = mn1 == -INFINITY ? 0.f : mn1;
+        al0 = exp2f(m[nt][0] - q0);
+        al1 = exp2f(m[nt][1] - q1);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+#pragma unroll
+        for (int dd = 0; dd < C::KS; ++dd) {
+          o[nt][dd][0] *= al0;
+          o[nt][dd][1] *= al1;
+          o[nt][dd][2] *= al0;
+          o[nt][dd][3] *= al1;
+        }
       }
-      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-      const float r0 = mn0 == -INFINITY ? 0.f : mn0, r1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m[nt][0] - r0), al1 = exp2f(m[nt][1] - r1);
-      m[nt][0] = mn0;
-      m[nt][1] = mn1;
+      const float r0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+      const float r1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const float p0 = exp2f(x[mt][0] - r0), p1 = exp2f(x[mt][1] - r1);
-        const float p2 = exp2f(x[mt][2] - r0), p3 = exp2f(x[mt][3] - r1);
+        const float p0 = exp2f(x[nt][mt][0] - r0), p1 = exp2f(x[nt][mt][1] - r1);
+        const float p2 = exp2f(x[nt][mt][2] - r0), p3 = exp2f(x[nt][mt][3] - r1);
         ps0 += p0 + p2;
         ps1 += p1 + p3;
         // P^T[token][head] fragments -> P[head][token] as the B operand of PV
@@ -458,13 +487,6 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       }
       l[nt][0] = l[nt][0] * al0 + ps0;
       l[nt][1] = l[nt][1] * al1 + ps1;
-#pragma unroll
-      for (int dd = 0; dd < C::KS; ++dd) {
-        o[nt][dd][0] *= al0;
-        o[nt][dd][1] *= al1;
-        o[nt][dd][2] *= al0;
-        o[nt][dd][3] *= al1;
-      }
     }
 
     // ---- O^T[d][head] += V_tile^T . P^T, one MMA per d-block and row block
@@ -520,6 +542,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     __syncwarp();  // every lane is done with this slot before it is refilled
   }
   cp_async_wait<0>();
+
+  if (p.S == 1) pdl_launch_dependents();
 
   // ---- denominators: sum over the 8 lanes that share tig (different tokens)
 #pragma unroll
