@@ -481,6 +481,75 @@ def test_two_streams_with_their_own_workspaces(cuda_lib):
         assert ws is not None and cuda_lib.read_device_errors(ws, stream=st) == 0
 
 
+def test_dependent_calls_back_to_back(cuda_lib):
+    # Each call's query is the previous call's output, and a torch kernel rewrites a
+    # live cache row (K and V) before every call. The calls follow each other with
+    # programmatic dependent launch (a grid of single-split sequences lets the next
+    # kernel launch after its main loop, a split grid its merge grid at once) and
+    # share one workspace, so every call must still see the inputs of the kernels
+    # before it complete. The chain runs as plain launches and as a captured graph;
+    # both must equal, bit for bit, the chain with a device synchronisation between
+    # all steps.
+    case = pi.make_case(3, 16, 8, 128, 16, [4000, 700, 33], seed=29, device="cuda")
+    splits = [1, 4, 1, 0, 2, 1, 7]
+    blk = int(case.block_tables[1, 0])  # token 5 of sequence 1 lives in row 5 of this block
+    g = torch.Generator(device="cpu").manual_seed(29)
+    new_k = [torch.randn(8, 128, generator=g).to(case.k_cache.dtype).cuda() for _ in splits]
+    new_v = [torch.randn(8, 128, generator=g).to(case.v_cache.dtype).cuda() for _ in splits]
+    k0, v0, q0 = case.k_cache.clone(), case.v_cache.clone(), case.q.clone()
+    k, v, q = case.k_cache, case.v_cache, case.q
+    outs = [torch.empty_like(q) for _ in splits]
+    max_len = case.max_seq_len  # read on the host before any capture
+
+    def chain(sync):
+        x = q
+        for i, S in enumerate(splits):
+            k[blk, 5].copy_(new_k[i])
+            v[blk, 5].copy_(new_v[i])
+            if sync:
+                torch.cuda.synchronize()
+            cuda_lib.decode(x, k, v, case.block_tables, case.seq_lens, case.scale, out=outs[i],
+                            max_seq_len=max_len, splits=S, deterministic=True)
+            if sync:
+                torch.cuda.synchronize()
+            x = outs[i]
+
+    def restart():
+        k.copy_(k0)
+        v.copy_(v0)
+        q.copy_(q0)
+        for o in outs:
+            o.fill_(float("nan"))
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        chain(sync=True)  # also sizes the stream's default workspace before the capture
+        restart()
+        chain(sync=True)
+        ref = [o.clone() for o in outs]
+        restart()
+        chain(sync=False)
+        s.synchronize()
+        plain = [o.clone() for o in outs]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            chain(sync=False)
+        restart()
+        graph.replay()
+        s.synchronize()
+    for i, (r, a, b) in enumerate(zip(ref, plain, outs)):
+        assert torch.isfinite(r).all(), f"call {i}"
+        assert torch.equal(a, r), f"plain chain, call {i} (splits {splits[i]})"
+        assert torch.equal(b, r), f"graph chain, call {i} (splits {splits[i]})"
+    # the first call of the chain against the oracle on its inputs (the oracle reads the
+    # contiguous K/V, so the rewritten row goes there too)
+    case.K[1][5].copy_(new_k[0])
+    case.V[1][5].copy_(new_v[0])
+    assert_parity(to_np(ref[0]), oracle_case(case.to("cpu")), what="first call of the chain")
+    ws = cuda_lib.default_workspace(q.device, s)
+    assert ws is not None and cuda_lib.read_device_errors(ws, stream=s) == 0
+
+
 # ------------------------------------------------------------------ sliding window
 @pytest.mark.parametrize("W", [1, 16, 1000, 1024, 4096])
 def test_sliding_window(cuda_lib, W):
