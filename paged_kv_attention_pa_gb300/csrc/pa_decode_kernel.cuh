@@ -177,20 +177,26 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       const int c = nt * 8 + gid;
       const bool ok = c < cols;
       const size_t rowp = (qrow(ok ? c : 0) * D) / 2;  // in bf16/f16 pairs
-#pragma unroll
-      for (int kk = 0; kk < C::KS; ++kk) {
+      if constexpr (F8) {
         // fp8 caches feed K to the MMA in a permuted d order: fragment elements
         // {2tig, 2tig+1, 2tig+8, 2tig+9} of k-step kk hold d = 4 KS tig + 4kk + {0..3},
         // so that a lane's K bytes of a row are contiguous; q takes the same order and
-        // every dot product is unchanged.
-        const int i0 = F8 ? 2 * C::KS * tig + 2 * kk : kk * 8 + tig;
-        const int i1 = F8 ? 2 * C::KS * tig + 2 * kk + 1 : kk * 8 + 4 + tig;
-        qf[nt][kk][0] = ok ? __ldg(q32 + rowp + i0) : 0u;
-        qf[nt][kk][1] = ok ? __ldg(q32 + rowp + i1) : 0u;
-        if constexpr (F8 && !std::is_same_v<T, __half>) {  // queries as fp16 pairs
-          const float2 a0 = unpack2<T>(qf[nt][kk][0]), a1 = unpack2<T>(qf[nt][kk][1]);
-          qf[nt][kk][0] = pack2<__half>(a0.x, a0.y);
-          qf[nt][kk][1] = pack2<__half>(a1.x, a1.y);
+        // every dot product is unchanged. The lane's q words of the row are then
+        // contiguous too (2 KS words from word 2 KS tig): 16-byte loads.
+        const uint4* q4 = reinterpret_cast<const uint4*>(q32 + rowp) + (C::KS / 2) * tig;
+#pragma unroll
+        for (int j = 0; j < C::KS / 2; ++j) {
+          const uint4 v = ok ? __ldg(q4 + j) : make_uint4(0u, 0u, 0u, 0u);
+          qf[nt][2 * j][0] = v.x;
+          qf[nt][2 * j][1] = v.y;
+          qf[nt][2 * j + 1][0] = v.z;
+          qf[nt][2 * j + 1][1] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < C::KS; ++kk) {
+          qf[nt][kk][0] = ok ? __ldg(q32 + rowp + kk * 8 + tig) : 0u;
+          qf[nt][kk][1] = ok ? __ldg(q32 + rowp + kk * 8 + 4 + tig) : 0u;
         }
       }
     }
@@ -331,6 +337,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   for (int k = 0; k < C::DEPTH - 1; ++k)
     if (k >= ns) issue(k, pe[k], tq[k]);
   int next_entry = pe[C::DEPTH - 1];  // for the tile issued in the first loop iteration
+  if constexpr (F8 && !std::is_same_v<T, __half>) {
+    // bf16 queries as fp16 pairs for the fp8 path's fp16 MMAs. Converted only now:
+    // done in the prologue, the conversion made the warp wait for the query's round
+    // trip before it could issue its first copies.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int kk = 0; kk < C::KS; ++kk) {
+        const float2 a0 = unpack2<T>(qf[nt][kk][0]), a1 = unpack2<T>(qf[nt][kk][1]);
+        qf[nt][kk][0] = pack2<__half>(a0.x, a0.y);
+        qf[nt][kk][1] = pack2<__half>(a1.x, a1.y);
+      }
+  }
 
   // running state: this thread's heads are nt*8 + 2*tig + {0, 1}
   float m[NT][2], l[NT][2];
