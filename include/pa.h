@@ -25,6 +25,13 @@
  *    stream) on the device current to the calling thread inside this library
  *    (see pa_set_device). Host-side argument errors are returned synchronously
  *    and nothing is launched.
+ *  - Kernels are launched with programmatic stream serialization. Each one waits
+ *    for the kernel before it in the stream to complete (griddepcontrol.wait)
+ *    before reading any input, so inputs written by that kernel are safe. Each
+ *    one also lets the next kernel in the stream start early: a kernel that the
+ *    caller launches after a decode call with the programmatic-serialization
+ *    attribute must wait in the same way (cudaGridDependencySynchronize) before
+ *    it reads `out`; a kernel launched without the attribute needs nothing.
  *  - Layouts are dense, row-major, with no padding:
  *        q, out        [B, Hq, D]                       (dtype)
  *        k_cache,
