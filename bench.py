@@ -249,14 +249,14 @@ def load_peaks():
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
 # A capture holds only for the kernel sources it was taken on: when their SHA-256
 # differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "79a33df2480575d5b8bcbac3c641d26ae4c17ab3037419a735bd7106738d88dd"
+TRAFFIC_SOURCES_SHA256 = "319a912e62845c46acb169436ddb5afc93197b69939bc9e937df34125e7e7703"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
-    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537072213 + 1461504},
+    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537050453 + 1655296},
     # 24q/4kv, block 784, batch 1, 32768 tokens: three launches
-    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134300160 + 1048661},
+    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134301013 + 1008299},
     # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: three launches
-    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268611499 + 994389},
+    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268608597 + 943445},
 }
 
 
@@ -445,6 +445,17 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------- our arm
+def kernels_per_call(pa, c):
+    """Kernels one decode call launches: the decode grid, plus the merge grid when the
+    context is split, except for two splits at head_dim 128, which merge inside their
+    thread-block cluster (all such calls but fp8 ones with more than 16 columns)."""
+    S = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8,
+                total_tokens=c.total_tokens)[0]
+    cols = (c.Hq // c.Hkv) * c.rows
+    cluster_merge = S == 2 and c.D == 128 and not (KV_FP8 and cols > 16)
+    return 1 if S == 1 or cluster_merge else 2
+
+
 def steady_state_us(pa, cell, stream, reps_target_ms=3.0):
     """us/call of back-to-back calls rotating over cache copies (graph replay)."""
     n = len(cell.insts)
@@ -646,15 +657,12 @@ def run_ours(args, rank, world, local_rank):
                   f"({kv / 2**30:.2f} GiB of distinct KV per step)",
             "timed": "CUDA graph of the whole step, replayed K times, CUDA events",
             "kv_bytes_per_step": kv}),
-        "gpu_launches": sum(2 if pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len,
-                                         window=c.window, kv_fp8=KV_FP8,
-                                         total_tokens=c.total_tokens)[0] > 1 else 1
-                            for c in cells) * args.steps,
+        "gpu_launches": sum(kernels_per_call(pa, c) for c in cells) * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "traffic_source": traffic_note,
                      "peak_kind": peak_kind,
-                     "kernel": "pa::decode_kernel (+ pa::merge_kernel when split)",
+                     "kernel": "pa::decode_kernel (+ pa::merge_kernel when split in more than two)",
                      "alg_bytes_per_launch": round(alg / len(cells)),
                      "avg_launch_us": round(1e3 * ms_step_max / len(cells), 3),
                      "launch_timing": "timed region / decode calls (graph replay, "

@@ -85,6 +85,16 @@ struct Cfg {
   static_assert(DEPTH >= 2, "need at least two slots per warp");
 };
 
+// The two-split cluster merge: at head_dim 128, where one warp's ring region holds,
+// after the last warp's merged state, a split's whole output state ([GT][D] sums,
+// then GT maxima and GT denominators). (Compiled into the head_dim-256 kernels it
+// cost the hybrid layer ~0.2 us per call, which never splits in two.)
+template <int D, int NT, bool F8>
+__host__ __device__ constexpr bool cluster_merge_fits() {
+  using C = Cfg<D, NT, F8>;
+  return D == 128 && (8 * NT * (D + 6) + 8 * NT * D + 16 * NT) * 4 <= C::DEPTH * C::SLOT_BYTES;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
                "l"(src), "l"(pol)
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   // have streamed their tiles: the next call's CTAs, resident early on the SMs
   // this grid leaves idle, measured slower than a later launch.
   pdl_wait();
-  if (p.S > 1) pdl_launch_dependents();
+  if (p.S > 1 && !p.cmerge) pdl_launch_dependents();
 
   // ---- prologue: everything the first copies depend on is requested at once (one
   // round trip): the context length, the query fragments and, speculatively, the
@@ -204,13 +214,16 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
 
   // ---- context length, validated against the bounds the launch was planned for
   if constexpr (!WIN) validate_len();
-  if (L == 0) {  // empty context: zero rows, written once
+  if (L == 0 && !p.cmerge) {  // empty context: zero rows, written once
     if (split == 0)
       for (int i = threadIdx.x; i < cols * D; i += kThreads)
         out[qrow(i / D) * D + i % D] = from_f32<T>(0.f);
     return;
   }
-  if (t_lo + split * p.P >= L) return;  // this split lies past the sequence: nothing to do
+  // a split past the sequence has nothing to do (in a merging cluster it streams
+  // nothing and still meets its partner at the cluster barriers)
+  const bool past = t_lo + split * p.P >= L;
+  if (past && !p.cmerge) return;
   const int n_splits = (L - t_lo + p.P - 1) / p.P;
   // Work sharing among the splits of one (sequence, KV head). Every split streams
   // its static share; the tokens past the n static shares go out one tile at a
@@ -218,7 +231,9 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   // them and all end together. The merge kernel resets the counter.
   const bool steal = p.Ps < p.P && n_splits > 1;
   const int s_hi = steal ? min(L, s_lo + p.Ps) : min(L, t_lo + (split + 1) * p.P);
-  const int n_stat = (s_hi - s_lo + C::TW - 1) / C::TW;  // static tiles of the CTA (>= 1)
+  // static tiles of the CTA (>= 1 unless past the sequence: its s_lo counts static
+  // shares, which may start inside the context that the first split covers alone)
+  const int n_stat = past ? 0 : (s_hi - s_lo + C::TW - 1) / C::TW;
   const int ns = warp < n_stat ? (n_stat - warp + kWarps - 1) / kWarps : 0;  // this warp's
   const int dyn_lo = steal ? min(L, t_lo + n_splits * p.Ps) : L;
   const int n_dyn = (L - dyn_lo + C::TW - 1) / C::TW;  // shared tiles of the sequence
@@ -562,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   }
   cp_async_wait<0>();
 
-  if (p.S == 1) pdl_launch_dependents();
+  if (p.S == 1 || p.cmerge) pdl_launch_dependents();
 
   // ---- denominators: sum over the 8 lanes that share tig (different tokens)
 #pragma unroll
@@ -636,6 +651,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     }
     // cache values are stored values times v_scale (1 unless fp8); a column whose
     // row sees no token of this split has M = -inf and den = 0
+    if constexpr (cluster_merge_fits<D, NT, F8>()) {
+      if (p.cmerge) {  // this split's state for the cluster merge below
+        float* xb = wstate(kWarps - 1) + WSTATE;
+        float4* xv = reinterpret_cast<float4*>(xb + g * D + d0);
+        xv[0] = make_float4(v[0], v[1], v[2], v[3]);
+        xv[1] = make_float4(v[4], v[5], v[6], v[7]);
+        if (d0 == 0) {
+          xb[GT * D + g] = M;
+          xb[GT * D + GT + g] = den;
+        }
+        continue;
+      }
+    }
     if (single) {
       const float r = den > 0.f ? p.v_scale / den : 0.f;
       uint4 pk;
@@ -653,6 +681,41 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         p.ws_m[pidx * cols + g] = M;
         p.ws_l[pidx * cols + g] = den;
       }
+    }
+  }
+  if constexpr (cluster_merge_fits<D, NT, F8>()) {
+    if (p.cmerge) {
+      // The two splits of this (sequence, KV head) form one cluster: split 1's state
+      // is read from its shared memory (distributed shared memory) and merged here,
+      // so no partials reach global memory and no merge grid runs.
+      cluster_sync();  // both splits' states are complete
+      if (cluster_rank() == 0) {
+        if (p.Ps < p.P && threadIdx.x == 0) p.steal[(size_t)b * p.Hkv + kvh] = 0;  // no claims left
+        const float* xb = wstate(kWarps - 1) + WSTATE;
+        const uint32_t rx = dsmem_addr(smem_addr(xb), 1);
+        for (int it = threadIdx.x; it < cols * DV; it += kThreads) {
+          const int g = it / DV, d0 = (it % DV) * 8;
+          const float m0 = xb[GT * D + g], l0 = xb[GT * D + GT + g];
+          const float m1 = ld_dsmem_f32(rx + 4u * (GT * D + g));
+          const float l1 = ld_dsmem_f32(rx + 4u * (GT * D + GT + g));
+          const float M = fmaxf(m0, m1);
+          const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+          const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+          const float den = w0 * l0 + w1 * l1;
+          const float r = den > 0.f ? p.v_scale / den : 0.f;
+          const float4* x0 = reinterpret_cast<const float4*>(xb + g * D + d0);
+          const float4 a0 = x0[0], a1 = x0[1];
+          const uint32_t x1 = rx + 4u * (g * D + d0);
+          const float4 c0 = ld_dsmem_f4(x1), c1 = ld_dsmem_f4(x1 + 16u);
+          uint4 pk;
+          pk.x = pack2<T>((w0 * a0.x + w1 * c0.x) * r, (w0 * a0.y + w1 * c0.y) * r);
+          pk.y = pack2<T>((w0 * a0.z + w1 * c0.z) * r, (w0 * a0.w + w1 * c0.w) * r);
+          pk.z = pack2<T>((w0 * a1.x + w1 * c1.x) * r, (w0 * a1.y + w1 * c1.y) * r);
+          pk.w = pack2<T>((w0 * a1.z + w1 * c1.z) * r, (w0 * a1.w + w1 * c1.w) * r);
+          *reinterpret_cast<uint4*>(out + qrow(g) * D + d0) = pk;
+        }
+      }
+      cluster_sync();  // split 1's shared memory stays until split 0 has read it
     }
   }
 }
@@ -751,19 +814,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
 // ------------------------------------------------------------------ launch
 // Launch with programmatic stream serialization: the grid may start while the
 // previous kernel in the stream finishes; its pdl_wait() orders the reads.
+// cluster_x > 1 groups that many consecutive CTAs along x into a thread-block cluster.
 template <typename Kern>
 cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       const DecodeParams& p) {
+                       const DecodeParams& p, unsigned cluster_x = 1) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -782,10 +850,14 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  e = launch_pdl(decode_kernel<T, KV, D, NT, WIN>, dim3(p.S, p.Hkv, p.B), dim3(C::THREADS), C::SMEM, st, p);
+  // Two splits merge inside their cluster (no merge grid) when their states fit.
+  DecodeParams q = p;
+  q.cmerge = (p.S == 2 && cluster_merge_fits<D, NT, std::is_same_v<KV, fp8e4m3>>()) ? 1 : 0;
+  e = launch_pdl(decode_kernel<T, KV, D, NT, WIN>, dim3(q.S, q.Hkv, q.B), dim3(C::THREADS), C::SMEM, st, q,
+                 q.cmerge ? 2u : 1u);
   if (e != cudaSuccess) return e;
-  if (p.S > 1)
-    e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, p.Hq * p.q_len, p.B), dim3(256), 0, st, p);
+  if (q.S > 1 && !q.cmerge)
+    e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, q.Hq * q.q_len, q.B), dim3(256), 0, st, q);
   return e;
 }
 

@@ -72,6 +72,8 @@ struct DecodeParams {
   int window;         // > 0: attend to the last `window` tokens only
   int q_len;          // query rows per sequence (causal among themselves)
   int kv_fp8;         // caches hold FP8 E4M3 (k_scale is folded into scale_log2)
+  int cmerge;         // S == 2 launched as clusters of the two splits, which merge in
+                      // distributed shared memory (set by the launcher; no merge grid)
   float v_scale;      // cache V value = stored value * v_scale
   float scale_log2;   // scale * log2(e): scores live in the exp2 domain
 };

@@ -481,6 +481,47 @@ def test_two_streams_with_their_own_workspaces(cuda_lib):
         assert ws is not None and cuda_lib.read_device_errors(ws, stream=st) == 0
 
 
+@pytest.mark.parametrize("shape", ["d128", "hybrid", "fp8", "window", "rows"])
+def test_two_splits_merge_in_their_cluster(cuda_lib, shape):
+    # Two splits run as one thread-block cluster and merge in distributed shared
+    # memory, with no merge grid (head_dim 128; the head_dim-256 shape takes the merge
+    # grid, and must pass the same checks). Edge cases: an empty context, contexts where the
+    # second split has no token (one of them, 1900, ends between the second split's
+    # static start and the partition size, where a split past the sequence would
+    # double-count tokens if it streamed its static share), a context shorter than a
+    # tile, and a long one whose splits share their tail.
+    lens = [0, 5, 33, 700, 1900, 4000]
+    kw = dict(splits=2)
+    if shape == "hybrid":
+        case = pi.make_case(6, 24, 4, 256, 784, lens, seed=31, poison="kv_nan")
+    elif shape == "fp8":
+        case = pi.make_case(6, 32, 8, 128, 16, lens, seed=32, poison="kv_nan", kv_dtype="fp8")
+    else:
+        case = pi.make_case(6, 32, 16, 128, 16, lens, seed=33, poison="kv_nan")
+    if shape == "window":
+        kw["window"] = 1024
+    if shape == "rows":
+        case = rows_case(3, 6, 32, 16, 128, 16, lens, seed=34, poison="kv_nan")
+        y = run(cuda_lib, case, **kw)
+        ref = oracle_rows_case(case)
+        assert_parity(to_np(y), ref, what="two splits, query rows")
+    else:
+        y = run(cuda_lib, case, **kw)
+        ref = oracle_case(case, window=kw.get("window", 0))
+        assert_parity(to_np(y), ref, what=f"two splits, {shape}")
+    assert torch.isfinite(y).all()
+    assert float(y[0].abs().max()) == 0.0  # the empty context
+    # the same call through the merge grid (three splits) agrees
+    kw3 = dict(kw, splits=3)
+    y3 = run(cuda_lib, case, **kw3)
+    assert rel_diff(y, y3) <= ORDER_TOL
+    # and in deterministic mode repeated calls are bit-identical
+    a = run(cuda_lib, case, deterministic=True, **kw)
+    b = run(cuda_lib, case, deterministic=True, **kw)
+    assert torch.equal(a, b)
+    no_device_errors(cuda_lib)
+
+
 def test_dependent_calls_back_to_back(cuda_lib):
     # Each call's query is the previous call's output, and a torch kernel rewrites a
     # live cache row (K and V) before every call. The calls follow each other with
