@@ -39,3 +39,25 @@ def test_traffic_is_null_once_the_device_code_changes(monkeypatch):
 def test_captures_read_each_kv_byte_about_once():
     for (D, kv), cap in bench.TRAFFIC_CAPTURES.items():
         assert 1.0 <= cap["dram_bytes"] / cap["alg_bytes"] < 1.02, (D, kv)
+
+
+def test_kernels_per_call_follows_the_split_plan(monkeypatch):
+    # one launch without a split; two splits at head_dim 128 merge in their clusters
+    # (one launch); more splits, or two at head_dim 256, add the merge grid
+    import paged_kv_attention_pa_gb300 as pa
+
+    class Cell:
+        def __init__(self, B, Hq, Hkv, D, bs, L, rows=1):
+            self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
+            self.max_len, self.window, self.total_tokens, self.rows = L, 0, 0, rows
+
+    splits = {}
+    monkeypatch.setattr(pa, "plan", lambda B, Hq, Hkv, D, bs, L, **kw: (splits[(D, L)], 64))
+    monkeypatch.setattr(bench, "KV_FP8", False)
+    for (D, S, n) in [(128, 1, 1), (128, 2, 1), (128, 3, 2), (256, 2, 2), (256, 38, 2)]:
+        splits[(D, 4096)] = S
+        assert bench.kernels_per_call(pa, Cell(8, 32, 8, D, 16, 4096)) == n, (D, S)
+    monkeypatch.setattr(bench, "KV_FP8", True)
+    splits[(128, 4096)] = 2
+    assert bench.kernels_per_call(pa, Cell(8, 32, 8, 128, 16, 4096)) == 1
+    assert bench.kernels_per_call(pa, Cell(8, 64, 8, 128, 16, 4096, rows=3)) == 2  # 24 columns
