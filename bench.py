@@ -249,7 +249,7 @@ def load_peaks():
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
 # A capture holds only for the kernel sources it was taken on: when their SHA-256
 # differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "319a912e62845c46acb169436ddb5afc93197b69939bc9e937df34125e7e7703"
+TRAFFIC_SOURCES_SHA256 = "019b8f9486200e6e7d1d6894a9481718d86e1c6a78e987e4bd7ce29d1ec846f9"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
     (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537050453 + 1655296},

@@ -29,10 +29,11 @@
 // fragments.
 //
 // Epilogue: the warps merge their (m, l, acc) in shared memory. A sequence that
-// fits in one split gets its output written here; otherwise the split's partial
-// goes to the workspace and merge_kernel, chained behind this grid with a
-// programmatic dependent launch, combines the splits of every (sequence, head)
-// in parallel.
+// fits in one split gets its output written here. Two splits at head_dim 128 run
+// as one thread-block cluster and merge through distributed shared memory.
+// Otherwise the split's partial goes to the workspace and merge_kernel, chained
+// behind this grid with a programmatic dependent launch, combines the splits of
+// every (sequence, head) in parallel.
 #pragma once
 
 #include <cstdint>
