@@ -36,6 +36,7 @@ import os
 import re
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -318,7 +319,9 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples: PA_BENCH_CLOCKS_DIR if set, else the system's temporary folder
+        out_dir = os.environ.get("PA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"pa_bench_clocks_gpu{index}_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -342,7 +345,11 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        if not os.environ.get("PA_BENCH_CLOCKS_DIR"):
+            os.remove(self.path)  # a temporary file unless the caller asked to keep it
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
