@@ -755,6 +755,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   }
   pdl_wait();  // the partials of the decode grid are complete and visible
   pdl_launch_dependents();
+  // One round trip: the context length, this thread's accumulators of splits sl + 4 i
+  // (i < 16) and the warp's maxima and sums of splits lane and lane + 32, all within
+  // the S splits launched. Splits past this sequence's own count wrote nothing: their
+  // slots hold stale values, replaced by select once the count is known.
+  float av[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int s2 = sl + 4 * i;
+    av[i] = s2 < p.S ? __ldcg(acc + (size_t)s2 * cols * D) : 0.f;
+  }
+  float mr[kReg], lr[kReg];
+#pragma unroll
+  for (int j = 0; j < kReg; ++j) {
+    const int s2 = lane + 32 * j;
+    mr[j] = s2 < p.S ? __ldcg(pm + (size_t)s2 * cols) : -INFINITY;
+    lr[j] = s2 < p.S ? __ldcg(pl + (size_t)s2 * cols) : 0.f;
+  }
   int L = __ldg(p.seq_lens + b);
   const int cap = (int)min((long long)p.max_seq_len, (long long)p.max_blocks * p.block_size);
   L = L < 0 ? 0 : (L > cap ? cap : L);
@@ -764,21 +781,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   // the decode grid is done with this (sequence, KV head)'s tile counter: rearm it
   if (p.Ps < p.P && blockIdx.x == 0 && row == 0 && g == 0 && threadIdx.x == 0)
     p.steal[(size_t)b * p.Hkv + kvh] = 0;
-
-  // One round trip: this thread's accumulators of splits sl + 4 i (i < 16) and the
-  // warp's maxima and sums of splits lane and lane + 32.
-  float av[kPre];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    const int s2 = sl + 4 * i;
-    av[i] = s2 < n ? __ldcg(acc + (size_t)s2 * cols * D) : 0.f;
-  }
-  float mr[kReg], lr[kReg];
+  for (int i = 0; i < kPre; ++i) av[i] = sl + 4 * i < n ? av[i] : 0.f;
 #pragma unroll
   for (int j = 0; j < kReg; ++j) {
-    const int s2 = lane + 32 * j;
-    mr[j] = s2 < n ? __ldcg(pm + (size_t)s2 * cols) : -INFINITY;
-    lr[j] = s2 < n ? __ldcg(pl + (size_t)s2 * cols) : 0.f;
+    const bool live = lane + 32 * j < n;
+    mr[j] = live ? mr[j] : -INFINITY;
+    lr[j] = live ? lr[j] : 0.f;
   }
   float M = fmaxf(mr[0], mr[1]);
   for (int s2 = lane + 32 * kReg; s2 < n; s2 += 32) M = fmaxf(M, __ldcg(pm + (size_t)s2 * cols));
