@@ -220,6 +220,25 @@ pa_status pa_set_device(int device) {
   return PA_OK;
 }
 
+// Division by the block size as a multiply-high and a shift (division by invariant
+// integers using multiplication, Granlund and Montgomery, 1994): for d not a power
+// of two, with l = ceil(log2 d), s = l - 1 and m = ceil(2^(32+s) / d) < 2^32,
+// floor(n m / 2^(32+s)) = floor(n / d) for every 0 <= n < 2^31, since the error
+// n (m d - 2^(32+s)) / (d 2^(32+s)) < 2^31 d / (d 2^(32+s)) <= 1/d.
+static void set_block_division(int d, uint32_t* magic, int* shift) {
+  int l = 0;
+  while ((1ll << l) < d) ++l;  // ceil(log2 d)
+  if ((1ll << l) == d) {       // a power of two: a shift
+    *magic = 0;
+    *shift = l;
+    return;
+  }
+  const int s = l - 1;
+  const unsigned long long num = 1ull << (32 + s);
+  *magic = (uint32_t)((num + (unsigned long long)d - 1) / (unsigned long long)d);
+  *shift = s;
+}
+
 pa_status pa_decode_plan(const pa_decode_args* a, int sm_count, int* splits,
                          int* partition_tokens) {
   if (!a || !splits || !partition_tokens) return PA_ERR_INVALID_ARG;
@@ -324,6 +343,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   p.Hkv = a->Hkv;
   p.G = G;
   p.block_size = a->block_size;
+  set_block_division(a->block_size, &p.bs_magic, &p.bs_shift);
   p.num_blocks = a->num_blocks;
   p.max_blocks = a->max_blocks_per_seq;
   p.max_seq_len = (int)max_len;

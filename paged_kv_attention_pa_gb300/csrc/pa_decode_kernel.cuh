@@ -90,6 +90,11 @@ struct Cfg {
 // after the last warp's merged state, a split's whole output state ([GT][D] sums,
 // then GT maxima and GT denominators). (Compiled into the head_dim-256 kernels it
 // cost the hybrid layer ~0.2 us per call, which never splits in two.)
+// t / block_size for a token index 0 <= t < 2^31 (see bs_magic)
+__device__ __forceinline__ int div_block(const DecodeParams& p, int t) {
+  return p.bs_magic == 0 ? (t >> p.bs_shift) : (int)(__umulhi((uint32_t)t, p.bs_magic) >> p.bs_shift);
+}
+
 template <int D, int NT, bool F8>
 __host__ __device__ constexpr bool cluster_merge_fits() {
   using C = Cfg<D, NT, F8>;
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   auto entry_of = [&](int t0) -> int {
     const long long t = (long long)t0 + lane;
     if (lane >= C::TW || t0 < 0 || t >= cap) return 0;
-    return __ldg(bt_row + (int)t / p.block_size);
+    return __ldg(bt_row + div_block(p, (int)t));
   };
   int pe[C::DEPTH];  // entries of tiles 0 .. DEPTH-1
 #pragma unroll
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       uint32_t ridx = 0;
       if (lane < nv) {
         const int t = t0 + lane;
-        const int off = t - (t / p.block_size) * p.block_size;
+        const int off = t - div_block(p, t) * p.block_size;
         if ((unsigned)phys >= (unsigned)p.num_blocks) {
           atomicOr(p.err, PA_DEVERR_BLOCK_INDEX);
           phys = 0;

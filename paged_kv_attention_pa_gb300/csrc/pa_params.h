@@ -67,6 +67,10 @@ struct DecodeParams {
   int* steal;         // [B*Hkv] claimed shared tiles per (sequence, KV head); zero between calls
   int B, Hq, Hkv, G;
   int block_size, num_blocks, max_blocks, max_seq_len;
+  // t / block_size for 0 <= t < 2^31 without a division: (t >> bs_shift) for a
+  // power of two (bs_magic == 0), else umulhi(t, bs_magic) >> bs_shift
+  uint32_t bs_magic;
+  int bs_shift;
   int S, P;           // splits and tokens per split
   int Ps;             // static tokens per split (== P: no shared tiles)
   int window;         // > 0: attend to the last `window` tokens only
