@@ -367,6 +367,78 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons of one GPU, read through NVML (ctypes, read-only
+    queries) every ~2 ms on a background thread, so that a timed region of a few tens
+    of milliseconds still holds many samples. start() returns False where NVML cannot
+    be loaded; the caller then falls back to nvidia-smi."""
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, device, period_s=0.002):
+        self.device, self.period = device, period_s
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self.thread, self.stop_flag = None, False
+
+    def _handle(self, lib):
+        import ctypes
+        h = ctypes.c_void_p()
+        try:
+            pr = torch.cuda.get_device_properties(self.device)
+            bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.device.index or 0), ctypes.byref(h)) == 0:
+            return h
+        return None
+
+    def start(self):
+        import ctypes
+        import threading
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = self._handle(lib)
+            if h is None:
+                return False
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except Exception:
+            return False
+
+        def loop():
+            mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self.stop_flag:
+                if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) == 0:
+                    self.samples.append(float(mhz.value))
+                if reasons_fn(h, ctypes.byref(rs)) == 0:
+                    self.reasons |= int(rs.value)
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+        return True
+
+    def stop(self):
+        if self.thread is None:
+            return None
+        self.stop_flag = True
+        self.thread.join(timeout=5)
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for n, bit in self.REASON_BITS.items() if self.reasons & bit),
+                "samples": len(self.samples), "source": "nvml every ~2 ms"}
+
+
 def cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -494,6 +566,63 @@ def steady_state_us(pa, cell, stream, reps_target_ms=3.0):
     return 1e3 * ms
 
 
+def attach_workspaces(pa, lib, cells, dev):
+    """One zeroed workspace per cell, so that a captured graph has fixed addresses."""
+    import ctypes
+    for c in cells:
+        x = c.insts[0]
+        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len, 0, c.window,
+                         FP8_SCALE, FP8_SCALE, total_tokens=c.total_tokens)
+        nbytes = lib.pa_decode_ex_workspace_bytes(ctypes.byref(a))
+        c.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+
+
+def measure_curve(pa, cells, stream, peak):
+    """Steady-state µs/call of every cell (or group: the hybrid's 16 layers of one
+    context length form one decode step), outside the timed region."""
+    curve = []
+    groups = {}
+    for c in cells:  # the hybrid's 16 layers of one length form one group
+        key = c.tag.split(" layer=")[0]
+        groups.setdefault(key, []).append(c)
+    for key, members in groups.items():
+        c = members[0]
+        c.add_copies(max(1, min(256, -(-ROTATE_BYTES // max(1, c.kv_bytes())))))
+        us = steady_state_us(pa, c, stream)
+        gbs = c.kv_bytes() / (us * 1e-6) / 1e9
+        S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8,
+                       total_tokens=c.total_tokens)
+        entry = {"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
+                 "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)}
+        if len(members) == 16:
+            # the hybrid's 16 full-attention layers are one decode step; its calls are
+            # independent, so the step is 16 back-to-back calls over distinct caches
+            entry["ms_per_step_16_layers"] = round(16 * us / 1000.0, 4)
+        curve.append(entry)
+        del c.insts[1:]
+        torch.cuda.empty_cache()
+    return curve
+
+
+def curve_summary(curve):
+    """The batch-1 and mixed-batch cells of the curve by context length."""
+    out = {}
+    for c in curve:
+        m = re.match(r"hybrid L=(\d+)$", c["cell"])
+        if m:
+            out.setdefault("hybrid_us_per_call", {})[m.group(1)] = c["us_per_call"]
+            out.setdefault("hybrid_frac", {})[m.group(1)] = c["frac"]
+            out.setdefault("hybrid_ms_per_step_16_layers", {})[m.group(1)] = \
+                c.get("ms_per_step_16_layers")
+        m = re.match(r"(\d+/\d+) B=1 L=(\d+)$", c["cell"])
+        if m:
+            out.setdefault(f"batch1_{m.group(1)}_frac", {})[m.group(2)] = c["frac"]
+        if c["cell"].startswith("mixed"):
+            out["mixed_frac"] = c["frac"]
+            out["mixed_us_per_call"] = c["us_per_call"]
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import ctypes
     import paged_kv_attention_pa_gb300 as pa
@@ -506,13 +635,7 @@ def run_ours(args, rank, world, local_rank):
     cells, desc = build_workload(args.workload, dev, seed=args.seed + 1000 * rank,
                                  cell_spec=args.cell)
     stream = torch.cuda.Stream(dev)
-    # one workspace per cell so the captured graph has fixed addresses
-    for c in cells:
-        x = c.insts[0]
-        a = pa.make_args(x.q, x.k, x.v, x.bt, x.sl, x.out, c.scale, c.max_len, 0, c.window,
-                         FP8_SCALE, FP8_SCALE, total_tokens=c.total_tokens)
-        nbytes = lib.pa_decode_ex_workspace_bytes(ctypes.byref(a))
-        c.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    attach_workspaces(pa, lib, cells, dev)
     torch.cuda.synchronize()
 
     def step_eager():
@@ -538,9 +661,12 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
 
     # ---------------- timed region: K graph replays
-    clocks = ClockSampler(dev.index) if rank == 0 else None
-    if clocks:
-        clocks.start()
+    clocks = None
+    if rank == 0:
+        clocks = NvmlSampler(dev)
+        if not clocks.start():
+            clocks = ClockSampler(dev.index)
+            clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -623,23 +749,16 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = load_peaks()
     curve = []
     if not args.no_curve:
-        groups = {}
-        for c in cells:  # the hybrid's 16 layers of one length form one group
-            key = c.tag.split(" layer=")[0]
-            groups.setdefault(key, []).append(c)
-        for key, members in groups.items():
-            c = members[0]
-            c.add_copies(max(1, min(256, -(-ROTATE_BYTES // max(1, c.kv_bytes())))))
-            us = steady_state_us(pa, c, stream)
-            gbs = c.kv_bytes() / (us * 1e-6) / 1e9
-            S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8,
-                           total_tokens=c.total_tokens)
-            entry = {"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
-                     "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)}
-            if len(members) == 16:  # the hybrid's 16 full-attention layers: one decode step
-                entry["ms_per_step_16_layers"] = round(16 * us / 1000.0, 4)
-            curve.append(entry)
-            del c.insts[1:]
+        curve = measure_curve(pa, cells, stream, peak)
+        if args.workload == "grid":
+            # Beside the grid: the hybrid full-attention layer (batch 1, 4 KV heads, head
+            # 256, block 784) at every context length as 16-layer steps, and the mixed
+            # serving batch, each in steady state like the grid's cells.
+            extra = build_workload("hybrid", dev, seed=args.seed + 5000)[0] + \
+                build_workload("mixed", dev, seed=args.seed)[0]
+            attach_workspaces(pa, lib, extra, dev)
+            curve += measure_curve(pa, extra, stream, peak)
+            del extra
             torch.cuda.empty_cache()
 
     linearity = hybrid_linearity(curve)
@@ -688,6 +807,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if linearity:
         line["linearity"] = linearity
+    if curve:
+        line["summary"] = curve_summary(curve)
     print(json.dumps(line), flush=True)
 
 

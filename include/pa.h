@@ -77,7 +77,6 @@ typedef enum pa_kv_dtype {
 /* Bits of the device error word (workspace header). */
 #define PA_DEVERR_BLOCK_INDEX 1u /* a live token's block table entry was outside [0, num_blocks) */
 #define PA_DEVERR_SEQ_LEN 2u     /* a seq_len < 0, > max_seq_len or > max_blocks_per_seq*block_size */
-#define PA_DEVERR_TIMEOUT 4u     /* reserved: a bounded wait gave up (no kernel spins today) */
 
 typedef void* pa_stream_t; /* cudaStream_t */
 
@@ -145,7 +144,9 @@ typedef struct pa_decode_args {
 #define PA_FLAG_DETERMINISTIC 1u
 
 /*
- * Workspace bytes pa_decode needs for these sizes on the current device. The
+ * Workspace bytes pa_decode needs for these sizes on the current device (the
+ * problem's sizes and the host-side bound on seq_lens; the split plan does not
+ * depend on the block size, so the query does not take one). The
  * workspace starts with a header of PA_WORKSPACE_HEADER_BYTES that must be zero
  * before the first call (pa_workspace_init or any memset): the device error word
  * (first 4 bytes) and one counter per (sequence, KV head) through which the
@@ -156,13 +157,17 @@ typedef struct pa_decode_args {
  * Returns 0 for invalid sizes (max_seq_len must be > 0 here).
  */
 #define PA_WORKSPACE_HEADER_BYTES 8448u
-size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size, int max_seq_len);
+size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_seq_len);
 
 /* Same, for pa_decode_ex's argument set (pointer fields are ignored). */
 size_t pa_decode_ex_workspace_bytes(const pa_decode_args* args);
 
 /*
- * Single-query paged-attention decode.
+ * Single-query paged-attention decode: the call of the problem statement in "vLLM's
+ * custom ROCm paged-attention kernel wins all sixty cells" (gqa-gate-costs-nothing),
+ * section 1 (one query token per sequence and head over a fully cached, block-paged
+ * context), with the split-KV partition and reduce of "Hybrid-SSM decode rate on dual
+ * Radeon cards under vLLM" (its split-KV paragraph) chosen inside the call.
  *   q             [B, Hq, D] queries (dtype)
  *   k_cache,
  *   v_cache       [num_blocks, block_size, Hkv, D] paged keys / values (dtype)
@@ -182,7 +187,10 @@ size_t pa_decode_ex_workspace_bytes(const pa_decode_args* args);
  *   workspace     device scratch of >= pa_decode_workspace_bytes(...) bytes,
  *                 256-byte aligned, its header zero before first use
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE,
- * PA_ERR_OUT_OF_RANGE (max_seq_len above capacity), PA_ERR_CUDA.
+ * PA_ERR_OUT_OF_RANGE (max_seq_len above capacity), PA_ERR_CUDA. On PA_ERR_CUDA a
+ * kernel of the call may already be queued; the call then also queues, behind it on
+ * `stream`, a clearing of the workspace header (tile counters and device error word),
+ * so that the workspace stays usable if the context does.
  */
 pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, const int32_t* seq_lens, void* out,
@@ -231,13 +239,18 @@ pa_status pa_set_device(int device);
  *  - Limit: a call whose partials need more than PA_NOALLOC_SCRATCH_BYTES (as
  *    pa_decode_workspace_bytes reports) returns PA_ERR_WORKSPACE and launches
  *    nothing; use pa_decode with your own workspace for it.
- *  - The first call on a device looks up the array's device address and zeroes
- *    its header (a synchronous cudaMemset); make that first call before any
- *    stream capture on that device.
+ *  - The first call on a device looks up the array's device address (once, kept
+ *    for the life of the process) and clears the array's header with an
+ *    asynchronous memset on `stream`, ordered before that call's kernels; make that
+ *    first call before any stream capture on that device. The address belongs to
+ *    the device's current context: after cudaDeviceReset on a device, this entry
+ *    point must not be called on it again in the same process.
  *  - Every call on a device shares the one array, which keeps the last call's
- *    contents. Nothing in it needs to start at zero except its header,
- *    cleared at that first call. Calls that may overlap on the GPU (different
- *    streams, concurrent threads) race on it: serialise them.
+ *    contents. Nothing in it needs to start at zero except its header (the tile
+ *    counters, which every successful call leaves at zero, and the error word).
+ *    Calls that may overlap on the GPU (different streams, concurrent threads)
+ *    race on it: serialise them. A call that returns PA_ERR_CUDA queues a clearing
+ *    of the header on `stream`, as pa_decode does for its workspace.
  *  - Device-side range errors (PA_DEVERR_*) are recorded in the array's header
  *    and are not readable through this API.
  */

@@ -28,15 +28,16 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, \
     PA_ERR_OUT_OF_RANGE = range(6)
 PA_F16, PA_BF16 = 0, 1
 PA_KV_AS_DTYPE, PA_KV_FP8_E4M3 = 0, 1
-PA_DEVERR_BLOCK_INDEX, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT = 1, 2, 4
+PA_DEVERR_BLOCK_INDEX, PA_DEVERR_SEQ_LEN = 1, 2
 PA_FLAG_DETERMINISTIC = 1
 PA_WORKSPACE_HEADER_BYTES = 8448
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 MAX_GQA_GROUP = 16
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _c = ctypes
 SIGNATURES = {
-    "pa_decode_workspace_bytes": (_c.c_size_t, [_c.c_int] * 6),
+    "pa_decode_workspace_bytes": (_c.c_size_t, [_c.c_int] * 5),
     "pa_decode_ex_workspace_bytes": (_c.c_size_t, [_c.c_void_p]),
     "pa_decode": (_c.c_int, [_c.c_void_p] * 6 + [_c.c_int] * 8 +
                   [_c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),

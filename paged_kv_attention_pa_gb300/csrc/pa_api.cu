@@ -263,19 +263,20 @@ size_t pa_decode_ex_workspace_bytes(const pa_decode_args* a) {
   return ws_layout(a->B, a->Hkv, (int64_t)(a->Hq / a->Hkv) * rows, a->D, S).total;
 }
 
-size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int block_size,
-                                 int max_seq_len) {
+size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_seq_len) {
+  // The plan depends on the sizes and the longest context, not on how the context is
+  // paged: any block size gives the same workspace, so one token per block stands in.
+  if (max_seq_len <= 0) return 0;
   pa_decode_args a{};
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.D = D;
-  a.block_size = block_size;
+  a.block_size = 1;
   a.num_blocks = 1;
-  a.max_blocks_per_seq = max_seq_len > 0 ? (int)ceil_div(max_seq_len, block_size > 0 ? block_size : 1) : 1;
+  a.max_blocks_per_seq = max_seq_len;
   a.max_seq_len = max_seq_len;
   a.dtype = PA_BF16;
-  if (max_seq_len <= 0) return 0;
   return pa_decode_ex_workspace_bytes(&a);
 }
 
@@ -381,6 +382,10 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
+    // A grid of this call may already be queued (the decode grid, when a later launch
+    // failed) and would leave its tile counters claimed: clear the header behind it
+    // on the same stream, so that the workspace still serves the next call.
+    if (cudaMemsetAsync(workspace, 0, pa::kHeaderBytes, cs) != cudaSuccess) cudaGetLastError();
     return PA_ERR_CUDA;
   }
   return PA_OK;

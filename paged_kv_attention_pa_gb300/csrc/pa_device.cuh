@@ -1,5 +1,6 @@
-// Device-side helpers for sm_103a: L2 cache policy, packed fp32x2 FMA, 16-bit
-// float unpacking. Inline PTX only; no library code.
+// Device-side helpers for sm_103a: L2 cache policy, fp8 widening, dependent-launch
+// and cluster primitives, 16-bit float packing, and the warp-level MMA / ldmatrix /
+// movmatrix wrappers. Inline PTX only; no library code.
 #pragma once
 
 #include <cstdint>
@@ -93,29 +94,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- fp32x2 FMA
-// d = a * b + c on two fp32 lanes at once (one packed instruction on sm_100+).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
-}
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  uint64_t ra, rb, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
-}
-
 // ---------------------------------------------------------------- 16-bit unpack
 // Two packed 16-bit floats (low half = element 0) to two fp32 values, exactly.
 template <typename T>
@@ -131,17 +109,6 @@ template <>
 __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
   __half2 h = *reinterpret_cast<__half2*>(&w);
   return __half22float2(h);
-}
-
-template <typename T>
-__device__ __forceinline__ float to_f32(T x);
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
-}
-template <>
-__device__ __forceinline__ float to_f32<__half>(__half x) {
-  return __half2float(x);
 }
 
 template <typename T>

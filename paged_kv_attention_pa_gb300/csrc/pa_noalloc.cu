@@ -24,9 +24,11 @@ std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of the array, per device
 
 // Once per device, with that device current: look up the array's device address
-// (the host-side name is only a stand-in, never a device pointer) and zero the
-// workspace header (the device error word and the shared-tile counters).
-pa_status scratch_for_current_device(void** out) {
+// (the host-side name is only a stand-in, never a device pointer). The array is
+// zero when the module loads; its header (the device error word and the tile
+// counters) is cleared once more on the caller's stream before the first launch,
+// so that the clearing is ordered before that launch whatever the stream.
+pa_status scratch_for_current_device(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -40,7 +42,7 @@ pa_status scratch_for_current_device(void** out) {
       cudaGetLastError();
       return PA_ERR_CUDA;
     }
-    if (cudaMemset(addr, 0, PA_WORKSPACE_HEADER_BYTES) != cudaSuccess) {
+    if (cudaMemsetAsync(addr, 0, PA_WORKSPACE_HEADER_BYTES, stream) != cudaSuccess) {
       cudaGetLastError();
       return PA_ERR_CUDA;
     }
@@ -76,11 +78,16 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_cache, const
   a.dtype = dtype;
   a.splits = 0;
   if (B == 0) return pa_decode_ex(&a, nullptr, 0, stream);  // validation only, no launch
-  void* scratch = nullptr;
-  const pa_status st = scratch_for_current_device(&scratch);
-  if (st != PA_OK) return st;
   const size_t need = pa_decode_ex_workspace_bytes(&a);
   if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;  // too big for the array
-  // need == 0 means invalid sizes: pa_decode_ex reports which.
+  if (need == 0) {
+    // invalid sizes (reported by pa_decode_ex, which launches nothing without a
+    // workspace), or no usable device
+    const pa_status st = pa_decode_ex(&a, nullptr, 0, stream);
+    return st == PA_ERR_WORKSPACE ? PA_ERR_CUDA : st;
+  }
+  void* scratch = nullptr;
+  const pa_status st = scratch_for_current_device((cudaStream_t)stream, &scratch);
+  if (st != PA_OK) return st;
   return pa_decode_ex(&a, scratch, PA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -72,7 +72,7 @@ int main(int argc, char** argv) {
     }
   }
   void *dq, *dk, *dv, *dbt, *dsl, *dout, *ws;
-  const size_t wsb = pa_decode_workspace_bytes(B, HQ, HKV, D, BS, 1000);
+  const size_t wsb = pa_decode_workspace_bytes(B, HQ, HKV, D, 1000);
   if (wsb == 0) return 3;
   CHECK(cudaMalloc(&dq, nq * 2));
   CHECK(cudaMalloc(&dk, nkv * 2));

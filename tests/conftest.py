@@ -29,3 +29,17 @@ def cuda_lib():
     import paged_kv_attention_pa_gb300 as pa
     pa.load()  # raises if the shared library is missing
     return pa
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest error against the float64 oracle that any parity check measured."""
+    try:
+        from harness import RECORDED
+    except Exception:
+        return
+    if not RECORDED:
+        return
+    what, err = max(RECORDED, key=lambda x: x[1])
+    terminalreporter.write_line(
+        f"parity: {len(RECORDED)} comparisons with the float64 oracle; largest rel L-inf "
+        f"error {err:.3e} ({what})")

@@ -57,11 +57,17 @@ def oracle_rows(case: PagedCase, pairs: Iterable[tuple]) -> dict:
     return out
 
 
+# Every error assert_parity measured in this process: (what, rel L-inf error). The
+# test session's summary reports the largest (tests/conftest.py).
+RECORDED: list = []
+
+
 def assert_parity(y: np.ndarray, r: np.ndarray, tol: float = REL_LINF_TOL, what: str = "") -> float:
-    """Every output finite and max|y-r|/max|r| <= tol. Returns the error."""
+    """Every output finite and max|y-r|/max|r| <= tol. Returns the error, and records it."""
     y = np.asarray(y, dtype=np.float64)
     assert np.all(np.isfinite(y)), f"{what}: non-finite output ({int((~np.isfinite(y)).sum())} values)"
     err = rel_linf_error(y, r)
+    RECORDED.append((what, float(err)))
     assert err <= tol, f"{what}: rel L-inf error {err:.3e} > {tol:.0e}"
     return err
 

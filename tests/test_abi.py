@@ -101,7 +101,7 @@ def test_workspace_header(lib):
     import torch
     if torch.cuda.is_available():  # sizes follow the current device's SM count
         for B, Hkv, L in [(1, 8, 512), (1, 4, 32768), (64, 8, 32768)]:
-            need = lib.pa_decode_workspace_bytes(B, 2 * Hkv, Hkv, 128, 16, L)
+            need = lib.pa_decode_workspace_bytes(B, 2 * Hkv, Hkv, 128, L)
             assert need >= pa.PA_WORKSPACE_HEADER_BYTES
     a = _args(flags=pa.PA_FLAG_DETERMINISTIC)
     assert lib.pa_decode_ex_workspace_bytes(ctypes.byref(a)) == \

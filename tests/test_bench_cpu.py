@@ -61,3 +61,17 @@ def test_kernels_per_call_follows_the_split_plan(monkeypatch):
     splits[(128, 4096)] = 2
     assert bench.kernels_per_call(pa, Cell(8, 32, 8, 128, 16, 4096)) == 1
     assert bench.kernels_per_call(pa, Cell(8, 64, 8, 128, 16, 4096, rows=3)) == 2  # 24 columns
+
+
+def test_curve_summary_picks_the_batch1_and_mixed_cells():
+    curve = [{"cell": "8/8 B=1 L=16384", "us_per_call": 14.0, "frac": 0.72},
+             {"cell": "8/8 B=8 L=16384", "us_per_call": 90.0, "frac": 0.9},
+             {"cell": "hybrid L=4096", "us_per_call": 6.0, "frac": 0.42,
+              "ms_per_step_16_layers": 0.096},
+             {"cell": "mixed B=64", "us_per_call": 700.0, "frac": 0.96}]
+    s = bench.curve_summary(curve)
+    assert s["batch1_8/8_frac"] == {"16384": 0.72}
+    assert s["hybrid_us_per_call"] == {"4096": 6.0}
+    assert s["hybrid_ms_per_step_16_layers"] == {"4096": 0.096}
+    assert s["mixed_frac"] == 0.96 and s["mixed_us_per_call"] == 700.0
+    assert "batch1_8/8_frac" in s and not any("B=8" in k for k in s)
