@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         }
         const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
         const float q0 = mn0 == -INFINITY ? 0.f : mn0, q1 = mn1 == -INFINITY ? 0.f : mn1;
-        al0 = exp2f(m[nt][0] - q0);
-        al1 = exp2f(m[nt][1] - q1);
+        al0 = exp2_approx(m[nt][0] - q0);
+        al1 = exp2_approx(m[nt][1] - q1);
         m[nt][0] = mn0;
         m[nt][1] = mn1;
 #pragma unroll
@@ -517,8 +517,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const float p0 = exp2f(x[nt][mt][0] - r0), p1 = exp2f(x[nt][mt][1] - r1);
-        const float p2 = exp2f(x[nt][mt][2] - r0), p3 = exp2f(x[nt][mt][3] - r1);
+        const float p0 = exp2_approx(x[nt][mt][0] - r0), p1 = exp2_approx(x[nt][mt][1] - r1);
+        const float p2 = exp2_approx(x[nt][mt][2] - r0), p3 = exp2_approx(x[nt][mt][3] - r1);
         ps0 += p0 + p2;
         ps1 += p1 + p3;
         // P^T[token][head] fragments -> P[head][token] as the B operand of PV
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
       const float* st = wstate(w);
       const float mwg = st[g];
       // a warp that saw no token of the column (m = -inf) contributes nothing
-      const float f = mwg == -INFINITY ? 0.f : exp2f(mwg - M);
+      const float f = mwg == -INFINITY ? 0.f : exp2_approx(mwg - M);
       const float4* src = reinterpret_cast<const float4*>(st + 2 * GT + g * AP + d0);
       const float4 x = src[0], y = src[1];
       v[0] += f * x.x; v[1] += f * x.y; v[2] += f * x.z; v[3] += f * x.w;
@@ -705,8 +705,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
           const float m1 = ld_dsmem_f32(rx + 4u * (GT * D + g));
           const float l1 = ld_dsmem_f32(rx + 4u * (GT * D + GT + g));
           const float M = fmaxf(m0, m1);
-          const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
-          const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+          const float w0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M);
+          const float w1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M);
           const float den = w0 * l0 + w1 * l1;
           const float r = den > 0.f ? p.v_scale / den : 0.f;
           const float4* x0 = reinterpret_cast<const float4*>(xb + g * D + d0);
@@ -801,11 +801,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   float wr[kReg], den = 0.f;
 #pragma unroll
   for (int j = 0; j < kReg; ++j) {
-    wr[j] = M == -INFINITY ? 0.f : exp2f(mr[j] - M);
+    wr[j] = M == -INFINITY ? 0.f : exp2_approx(mr[j] - M);
     den += wr[j] * lr[j];
   }
   for (int s2 = lane + 32 * kReg; s2 < n; s2 += 32)
-    den += M == -INFINITY ? 0.f : exp2f(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(pl + (size_t)s2 * cols);
+    den += M == -INFINITY ? 0.f : exp2_approx(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(pl + (size_t)s2 * cols);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
 
@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
     num += __shfl_sync(0xffffffffu, wr[i / 8], s2 & 31) * av[i];
   }
   for (int s2 = sl + 4 * kPre; s2 < n; s2 += 4)
-    num += M == -INFINITY ? 0.f : exp2f(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(acc + (size_t)s2 * cols * D);
+    num += M == -INFINITY ? 0.f : exp2_approx(__ldcg(pm + (size_t)s2 * cols) - M) * __ldcg(acc + (size_t)s2 * cols * D);
   part[sl][dl] = num;
   __syncthreads();
   if (sl == 0) {

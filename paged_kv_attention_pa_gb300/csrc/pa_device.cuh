@@ -36,6 +36,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
   return y;
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32, relative error about
+// 2^-22). Every use here has x <= 0 (softmax weights, rescale factors): results lie
+// in [0, 1], subnormal ones flush to zero, and 2^-inf = +0.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Ask for the L2 line holding p (no data returned; a hint the memory system may drop).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
