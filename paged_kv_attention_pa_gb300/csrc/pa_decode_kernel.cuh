@@ -43,19 +43,6 @@
 #include "pa_device.cuh"
 #include "pa_params.h"
 
-#ifndef PA_WARPS_D128
-#define PA_WARPS_D128 4
-#endif
-#ifndef PA_WARPS_D256
-#define PA_WARPS_D256 4
-#endif
-#ifndef PA_WARPS_F8_D128
-#define PA_WARPS_F8_D128 8  // fp8 tiles cost more math per byte: more warps
-#endif
-#ifndef PA_WARPS_F8_D256
-#define PA_WARPS_F8_D256 4
-#endif
-
 namespace pa {
 
 constexpr int kSmemBudget = 224 * 1024;
@@ -64,8 +51,7 @@ constexpr int kSmemBudget = 224 * 1024;
 // bytes, and each lane widens the bytes of its MMA fragments in registers.
 template <int D, int NT, bool F8 = false>
 struct Cfg {
-  static constexpr int NW = D == 128 ? (F8 ? PA_WARPS_F8_D128 : PA_WARPS_D128)
-                                     : (F8 ? PA_WARPS_F8_D256 : PA_WARPS_D256);  // warps per CTA
+  static constexpr int NW = warps_per_cta(D, F8);  // warps per CTA
   static constexpr int THREADS = NW * 32;
   static constexpr int TW = tile_tokens(D, F8);  // tokens per tile
   static_assert(TW % 16 == 0 && TW <= 32, "a tile is whole MMA row blocks, one token per lane");

@@ -34,6 +34,23 @@ constexpr int tile_tokens(int D, bool fp8) {
   return fp8 ? (D == 128 ? PA_TILE_TOKENS_F8_D128 : PA_TILE_TOKENS_F8_D256)
              : (D == 128 ? PA_TILE_TOKENS_D128 : PA_TILE_TOKENS_D256);
 }
+// Warps per decode CTA, per head_dim and cache type: fp8 tiles cost more math per
+// byte, so the fp8 kernel at head_dim 128 runs more warps.
+#ifndef PA_WARPS_D128
+#define PA_WARPS_D128 4
+#endif
+#ifndef PA_WARPS_D256
+#define PA_WARPS_D256 4
+#endif
+#ifndef PA_WARPS_F8_D128
+#define PA_WARPS_F8_D128 8
+#endif
+#ifndef PA_WARPS_F8_D256
+#define PA_WARPS_F8_D256 4
+#endif
+constexpr int warps_per_cta(int D, bool fp8) {
+  return D == 128 ? (fp8 ? PA_WARPS_F8_D128 : PA_WARPS_D128) : (fp8 ? PA_WARPS_F8_D256 : PA_WARPS_D256);
+}
 // Work sharing among the splits of a sequence: each split keeps about
 // (1 - 1/kStealDiv) of its P tokens as a static share, and the rest of the context
 // is claimed tile by tile through one counter per (sequence, KV head) held in the
