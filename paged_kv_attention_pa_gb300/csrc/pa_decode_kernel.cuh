@@ -453,16 +453,31 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     float x[NT][MT][4];
     float mx[NT][2];
     bool grow = false;  // some column of this lane sees a score above its running max
+    if (t0 + C::TW <= L - R + 1) {
+      // every token of the tile is below every column's limit (the usual case): no mask
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[nt][mt][i] = (s[mt][nt][i] + s2[mt][nt][i]) * sl2;
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int tok0 = t0 + 16 * mt + gid, tok1 = tok0 + 8;
+          x[nt][mt][0] = tok0 < lim[nt][0] ? (s[mt][nt][0] + s2[mt][nt][0]) * sl2 : -INFINITY;
+          x[nt][mt][1] = tok0 < lim[nt][1] ? (s[mt][nt][1] + s2[mt][nt][1]) * sl2 : -INFINITY;
+          x[nt][mt][2] = tok1 < lim[nt][0] ? (s[mt][nt][2] + s2[mt][nt][2]) * sl2 : -INFINITY;
+          x[nt][mt][3] = tok1 < lim[nt][1] ? (s[mt][nt][3] + s2[mt][nt][3]) * sl2 : -INFINITY;
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       mx[nt][0] = mx[nt][1] = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int tok0 = t0 + 16 * mt + gid, tok1 = tok0 + 8;
-        x[nt][mt][0] = tok0 < lim[nt][0] ? (s[mt][nt][0] + s2[mt][nt][0]) * sl2 : -INFINITY;
-        x[nt][mt][1] = tok0 < lim[nt][1] ? (s[mt][nt][1] + s2[mt][nt][1]) * sl2 : -INFINITY;
-        x[nt][mt][2] = tok1 < lim[nt][0] ? (s[mt][nt][2] + s2[mt][nt][2]) * sl2 : -INFINITY;
-        x[nt][mt][3] = tok1 < lim[nt][1] ? (s[mt][nt][3] + s2[mt][nt][3]) * sl2 : -INFINITY;
         mx[nt][0] = fmaxf(mx[nt][0], fmaxf(x[nt][mt][0], x[nt][mt][2]));
         mx[nt][1] = fmaxf(mx[nt][1], fmaxf(x[nt][mt][1], x[nt][mt][3]));
       }
@@ -529,11 +544,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         for (int j = 0; j < 4; ++j) {
           const int r = 16 * mt + 2 * tig + (j & 1) + 8 * (j >> 1);
 #pragma unroll
-          for (int u = 0; u < C::KS / 8; ++u) {
-            const uint4 x = lds128(vt + r * C::ROWB + 2 * C::KS * gid + 16 * u);
-            vw[mt][j][u] = r < nv ? x : make_uint4(0u, 0u, 0u, 0u);
-          }
+          for (int u = 0; u < C::KS / 8; ++u) vw[mt][j][u] = lds128(vt + r * C::ROWB + 2 * C::KS * gid + 16 * u);
         }
+      if (nv < C::TW) {  // a partial tile: its rows past seq_len were never loaded
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 16 * mt + 2 * tig + (j & 1) + 8 * (j >> 1);
+#pragma unroll
+            for (int u = 0; u < C::KS / 8; ++u)
+              if (r >= nv) vw[mt][j][u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+      }
 #pragma unroll
       for (int dd = 0; dd < C::KS; ++dd) {
         const int wi = dd >> 1;                             // word of bytes 2dd, 2dd + 1
