@@ -163,15 +163,18 @@ def parse_cell(spec):
     return hq, hkv, B, L, D, bs
 
 
-def build_workload(name, device, seed=0, cell_spec=None):
+def build_workload(name, device, seed=0, cell_spec=None, fp8=None, lens=None):
+    """The cells of a workload. fp8 overrides --kv-dtype for these cells (their tags
+    then start with 'fp8 '); lens restricts the hybrid layer's context lengths."""
     cells = []
+    pre = "fp8 " if fp8 else ""
     if name == "grid":
         i = 0
         for B in GRID_BATCHES:
             for hq, hkv in GRID_SHAPES:
                 for L in GRID_LENS:
                     cells.append(Cell(B, hq, hkv, 128, 16, [L] * B, seed + i, device,
-                                      tag=f"{hq}/{hkv} B={B} L={L}"))
+                                      tag=f"{pre}{hq}/{hkv} B={B} L={L}", fp8=fp8))
                     i += 1
         desc = {"workload": "gqa_depth_grid", "head_dim": 128, "block_size": 16,
                 "shapes_hq_hkv": GRID_SHAPES, "seq_lens": GRID_LENS, "batches": GRID_BATCHES,
@@ -179,10 +182,10 @@ def build_workload(name, device, seed=0, cell_spec=None):
     elif name == "hybrid":
         # 16 independent layer caches per context length: 24q/4kv, head 256, block 784
         i = 0
-        for L in HYBRID_LENS:
+        for L in (lens or HYBRID_LENS):
             for layer in range(16):
                 cells.append(Cell(1, 24, 4, 256, 784, [L], seed + i, device,
-                                  tag=f"hybrid L={L} layer={layer}"))
+                                  tag=f"{pre}hybrid L={L} layer={layer}", fp8=fp8))
                 i += 1
         desc = {"workload": "hybrid_full_attention_layer", "Hq": 24, "Hkv": 4, "head_dim": 256,
                 "block_size": 784, "batch": 1, "seq_lens": HYBRID_LENS, "layers_per_step": 16,
@@ -590,7 +593,7 @@ def measure_curve(pa, cells, stream, peak):
         c.add_copies(max(1, min(256, -(-ROTATE_BYTES // max(1, c.kv_bytes())))))
         us = steady_state_us(pa, c, stream)
         gbs = c.kv_bytes() / (us * 1e-6) / 1e9
-        S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8,
+        S, P = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=c.fp8,
                        total_tokens=c.total_tokens)
         entry = {"cell": key, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
                  "frac": round(gbs / peak, 4), "splits": S, "copies": len(c.insts)}
@@ -620,7 +623,39 @@ def curve_summary(curve):
         if c["cell"].startswith("mixed"):
             out["mixed_frac"] = c["frac"]
             out["mixed_us_per_call"] = c["us_per_call"]
+        m = re.match(r"fp8 hybrid L=(\d+)$", c["cell"])
+        if m:
+            out.setdefault("fp8_hybrid_us_per_call", {})[m.group(1)] = c["us_per_call"]
+            out.setdefault("fp8_hybrid_frac", {})[m.group(1)] = c["frac"]
+    for L, us in out.get("fp8_hybrid_us_per_call", {}).items():
+        bf = out.get("hybrid_us_per_call", {}).get(L)
+        if bf:
+            out.setdefault("fp8_over_bf16_hybrid_time", {})[L] = round(us / bf, 3)
     return out
+
+
+def time_step(pa, cells, stream, steps, warmup):
+    """ms per step of all cells' calls captured as one CUDA graph (CUDA events on the
+    launching stream, `steps` replays after `warmup`)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c in cells:
+            c.call(pa, stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for c in cells:
+                c.call(pa, stream)
+        for _ in range(warmup):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+    del g
+    return e0.elapsed_time(e1) / steps
 
 
 def run_ours(args, rank, world, local_rank):
@@ -748,6 +783,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- steady-state curve (outside the timed region)
     peak, peak_kind = load_peaks()
     curve = []
+    fp8_grid = None
     if not args.no_curve:
         curve = measure_curve(pa, cells, stream, peak)
         if args.workload == "grid":
@@ -759,6 +795,22 @@ def run_ours(args, rank, world, local_rank):
             attach_workspaces(pa, lib, extra, dev)
             curve += measure_curve(pa, extra, stream, peak)
             del extra
+            torch.cuda.empty_cache()
+            # FP8 E4M3 caches: the hybrid layer at 4K / 16K / 32K (steady state, as
+            # above) and the grid step (one graph of the 60 calls, like the headline)
+            extra = build_workload("hybrid", dev, seed=args.seed + 7000, fp8=True,
+                                   lens=[4096, 16384, 32768])[0]
+            attach_workspaces(pa, lib, extra, dev)
+            curve += measure_curve(pa, extra, stream, peak)
+            del extra
+            grid8 = build_workload("grid", dev, seed=args.seed + 9000, fp8=True)[0]
+            attach_workspaces(pa, lib, grid8, dev)
+            ms8 = time_step(pa, grid8, stream, max(args.steps, 10), args.warmup)
+            kv8 = sum(c.kv_bytes() for c in grid8)
+            fp8_grid = {"ms_per_step": round(ms8, 4), "kv_gbs": round(kv8 / (ms8 * 1e-3) / 1e9, 1),
+                        "frac": round(kv8 / (ms8 * 1e-3) / 1e9 / peak, 4),
+                        "kv_bytes_per_step": kv8}
+            del grid8
             torch.cuda.empty_cache()
 
     linearity = hybrid_linearity(curve)
@@ -809,6 +861,8 @@ def run_ours(args, rank, world, local_rank):
         line["linearity"] = linearity
     if curve:
         line["summary"] = curve_summary(curve)
+        if fp8_grid:
+            line["summary"]["fp8_grid_step"] = fp8_grid
     print(json.dumps(line), flush=True)
 
 

@@ -75,3 +75,15 @@ def test_curve_summary_picks_the_batch1_and_mixed_cells():
     assert s["hybrid_ms_per_step_16_layers"] == {"4096": 0.096}
     assert s["mixed_frac"] == 0.96 and s["mixed_us_per_call"] == 700.0
     assert "batch1_8/8_frac" in s and not any("B=8" in k for k in s)
+
+
+def test_curve_summary_reports_fp8_against_bf16():
+    curve = [{"cell": "hybrid L=32768", "us_per_call": 25.0, "frac": 0.8,
+              "ms_per_step_16_layers": 0.4},
+             {"cell": "fp8 hybrid L=32768", "us_per_call": 17.5, "frac": 0.57,
+              "ms_per_step_16_layers": 0.28}]
+    s = bench.curve_summary(curve)
+    assert s["hybrid_us_per_call"] == {"32768": 25.0}     # the fp8 cell is not a bf16 one
+    assert s["fp8_hybrid_us_per_call"] == {"32768": 17.5}
+    assert s["fp8_over_bf16_hybrid_time"] == {"32768": 0.7}
+    assert bench.hybrid_linearity(curve) is None            # fits only the bf16 cells
