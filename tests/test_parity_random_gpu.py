@@ -1,0 +1,107 @@
+"""Randomised parity sweep: the CUDA path against the float64 oracle (GB300 only).
+
+Each case draws, from a fixed seed, one point of the space the boundary accepts:
+batch, KV heads and query-head group (Hq / Hkv up to 16), head_dim 128 or 256,
+block size (1 up to 1024 tokens, powers of two or not), context lengths (empty,
+a single token, block-straddling, up to a few thousand), 16-bit query type, a
+16-bit or FP8 E4M3 cache, several causal query rows, a sliding window, a forced
+split count, the deterministic flag and one fill of the unwritten slots ("vLLM's
+custom ROCm paged-attention kernel wins all sixty cells", §1 for the problem,
+§5 for the fills). Every output is compared with the oracle at the parity bar.
+The draw is seeded, so a failing case is reproduced by its index.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import pa_inputs as pi
+from harness import assert_parity, oracle_case, oracle_rows_case
+
+N_CASES = 160
+BLOCK_SIZES = [1, 3, 16, 32, 33, 48, 128, 784, 1024]
+
+
+def draw(idx: int) -> dict:
+    """One seeded case: sizes and options within what the boundary accepts."""
+    r = random.Random(90210 + idx)
+    D = r.choice([128, 256])
+    Hkv = r.choice([1, 2, 4, 8])
+    fp8 = r.random() < 0.3
+    rows = r.choice([1, 1, 1, 2, 3]) if r.random() < 0.4 else 1
+    max_cols = 32 if D == 128 else 16
+    G = r.choice([g for g in (1, 2, 3, 4, 6, 8, 12, 16) if g * rows <= max_cols])
+    B = r.randint(1, 5)
+    bs = r.choice(BLOCK_SIZES)
+    lens = []
+    for _ in range(B):
+        kind = r.random()
+        if kind < 0.08:
+            lens.append(0)
+        elif kind < 0.16:
+            lens.append(1)
+        elif kind < 0.5:
+            k = r.randint(1, 64)  # a length that ends inside a block
+            lens.append(max(1, k * bs + r.randint(-bs + 1, bs - 1)) if bs > 1 else k * 37)
+        else:
+            lens.append(r.randint(2, 3000))
+    lens = [min(L, 4000) for L in lens]
+    window = r.choice([0, 0, 0, 1, 17, 512, 1024]) if rows == 1 else 0
+    return dict(B=B, Hq=G * Hkv, Hkv=Hkv, D=D, bs=bs, lens=lens, rows=rows, fp8=fp8,
+                dtype=r.choice(["bf16", "f16"]), window=window,
+                splits=r.choice([0, 0, 1, 2, 3, 5, 9]),
+                deterministic=r.random() < 0.3,
+                poison=r.choice(list(pi.POISON_MODES)), seed=idx)
+
+
+def build(cfg: dict):
+    case = pi.make_case(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["bs"], cfg["lens"],
+                        dtype=cfg["dtype"], seed=cfg["seed"], poison=cfg["poison"],
+                        kv_dtype="fp8" if cfg["fp8"] else None,
+                        table_fill=("oob" if cfg["seed"] % 2 else "neg1"))
+    if cfg["rows"] > 1:
+        g = torch.Generator().manual_seed(5000 + cfg["seed"])
+        B, Hq, D = case.q.shape
+        case.q = torch.randn((B, cfg["rows"], Hq, D), generator=g).to(case.q.dtype)
+    return case
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("idx", range(N_CASES))
+def test_random_case_matches_oracle(cuda_lib, idx):
+    cfg = draw(idx)
+    case = build(cfg)
+    ref = oracle_rows_case(case) if cfg["rows"] > 1 else oracle_case(case, window=cfg["window"])
+    c = case.to("cuda")
+    kw = dict(splits=cfg["splits"], window=cfg["window"], deterministic=cfg["deterministic"])
+    if c.kv_fp8:
+        kw.update(k_scale=c.k_scale, v_scale=c.v_scale)
+    max_len = max(cfg["lens"]) if max(cfg["lens"]) > 0 else None
+    out = cuda_lib.decode(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
+                          max_seq_len=max_len, **kw)
+    torch.cuda.synchronize()
+    y = out.detach().to("cpu", torch.float64).numpy()
+    what = f"case {idx}: {cfg}"
+    if np.abs(ref).max() == 0:  # every context empty (or every row sees no token)
+        assert np.all(y == 0), what
+    else:
+        assert_parity(y, ref, what=what)
+    ws = cuda_lib.default_workspace()
+    assert ws is not None and cuda_lib.read_device_errors(ws) == 0, what
+
+
+def test_draws_cover_the_space():
+    # CPU-side check of the draw itself: the sweep reaches every option it claims to
+    cfgs = [draw(i) for i in range(N_CASES)]
+    assert {c["D"] for c in cfgs} == {128, 256}
+    assert any(c["fp8"] for c in cfgs) and any(not c["fp8"] for c in cfgs)
+    assert any(c["rows"] > 1 for c in cfgs) and any(c["window"] > 0 for c in cfgs)
+    assert any(0 in c["lens"] for c in cfgs) and any(1 in c["lens"] for c in cfgs)
+    assert len({c["bs"] for c in cfgs}) >= 6
+    assert any(c["splits"] > 1 for c in cfgs) and any(c["deterministic"] for c in cfgs)
+    assert len({c["poison"] for c in cfgs}) == len(pi.POISON_MODES)
+    for c in cfgs:
+        cols = (c["Hq"] // c["Hkv"]) * c["rows"]
+        assert cols <= (32 if c["D"] == 128 else 16) and c["Hq"] // c["Hkv"] <= 16
+        assert not (c["rows"] > 1 and c["window"] > 0)
