@@ -528,14 +528,12 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------------- our arm
 def kernels_per_call(pa, c):
-    """Kernels one decode call launches: the decode grid, plus the merge grid when the
-    context is split, except for two splits at head_dim 128, which merge inside their
-    thread-block cluster (all such calls but fp8 ones with more than 16 columns)."""
-    S = pa.plan(c.B, c.Hq, c.Hkv, c.D, c.bs, c.max_len, window=c.window, kv_fp8=KV_FP8,
-                total_tokens=c.total_tokens)[0]
-    cols = (c.Hq // c.Hkv) * c.rows
-    cluster_merge = S == 2 and c.D == 128 and not (KV_FP8 and cols > 16)
-    return 1 if S == 1 or cluster_merge else 2
+    """Kernels one decode call of the cell launches, as the library reports it for the
+    cell's tensors on this device: the decode grid, plus the merge grid unless the
+    context fits one split or its splits merge inside their thread-block clusters."""
+    x = c.insts[0]
+    return pa.kernel_count(x.q, x.k, x.v, x.bt, x.sl, c.scale, max_seq_len=c.max_len,
+                           window=c.window, total_tokens=c.total_tokens)
 
 
 def steady_state_us(pa, cell, stream, reps_target_ms=3.0):

@@ -212,6 +212,15 @@ pa_status pa_decode_ex(const pa_decode_args* args, void* workspace, size_t works
 pa_status pa_decode_plan(const pa_decode_args* args, int sm_count, int* splits,
                          int* partition_tokens);
 
+/*
+ * How many kernels pa_decode_ex would launch for `args` on the current device (the
+ * plan, and whether the splits merge inside their thread-block clusters, depend on
+ * the device): 0 for B == 0, 1 for a context in one split or splits that merge in
+ * their cluster, 2 for a decode grid followed by a merge grid. Pointer fields are
+ * not read; nothing is launched. The same argument errors as pa_decode_ex.
+ */
+pa_status pa_decode_kernel_count(const pa_decode_args* args, int* kernels);
+
 /* Zero-fill a workspace on `stream` (asynchronous). */
 pa_status pa_workspace_init(void* workspace, size_t workspace_bytes, pa_stream_t stream);
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "pa_decode_noalloc": (_c.c_int, [_c.c_void_p] * 6 + [_c.c_int] * 8 +
                           [_c.c_float, _c.c_int, _c.c_void_p]),
     "pa_decode_plan": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_void_p, _c.c_void_p]),
+    "pa_decode_kernel_count": (_c.c_int, [_c.c_void_p, _c.c_void_p]),
     "pa_workspace_init": (_c.c_int, [_c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "pa_read_device_errors": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p]),
     "pa_set_device": (_c.c_int, [_c.c_int]),
@@ -289,6 +290,22 @@ def plan(B: int, Hq: int, Hkv: int, D: int, block_size: int, max_seq_len: int,
     if rc != PA_OK:
         raise PAError(rc, "pa_decode_plan")
     return S.value, P.value
+
+
+def kernel_count(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=None,
+                 splits: int = 0, window: int = 0, total_tokens: int = 0) -> int:
+    """Kernels one decode call with these tensors launches on their device (1, or 2
+    with a merge grid; 0 for an empty batch). Nothing is launched."""
+    lib = load()
+    out = q  # only its shape and dtype are read
+    args = make_args(q, k_cache, v_cache, block_tables, seq_lens, out, scale, max_seq_len,
+                     splits, window, total_tokens=total_tokens)
+    _ensure_device(lib, q.device.index)
+    n = ctypes.c_int(-1)
+    rc = lib.pa_decode_kernel_count(ctypes.byref(args), ctypes.byref(n))
+    if rc != PA_OK:
+        raise PAError(rc, "pa_decode_kernel_count")
+    return n.value
 
 
 def read_device_errors(workspace: torch.Tensor, stream=None) -> int:

@@ -303,18 +303,25 @@ pa_status pa_read_device_errors(void* workspace, pa_stream_t stream, uint32_t* f
   return PA_OK;
 }
 
-pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspace_bytes,
-                       pa_stream_t stream) {
+// The decode call, or (kernels != nullptr) only the count of kernels it would launch:
+// then no pointer is read and nothing is launched.
+static pa_status decode_ex(const pa_decode_args* a, void* workspace, size_t workspace_bytes,
+                           pa_stream_t stream, int* kernels) {
   if (!a) return PA_ERR_INVALID_ARG;
   int64_t max_len = 0;
   pa_status st = check_sizes(a, &max_len);
   if (st != PA_OK) return st;
-  if (a->B == 0) return PA_OK;  // nothing to compute
-  if (!a->q || !a->k_cache || !a->v_cache || !a->block_tables || !a->seq_lens || !a->out)
-    return PA_ERR_INVALID_ARG;
-  if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->out))
-    return PA_ERR_INVALID_ARG;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_WORKSPACE;
+  if (a->B == 0) {  // nothing to compute
+    if (kernels) *kernels = 0;
+    return PA_OK;
+  }
+  if (!kernels) {
+    if (!a->q || !a->k_cache || !a->v_cache || !a->block_tables || !a->seq_lens || !a->out)
+      return PA_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->out))
+      return PA_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_WORKSPACE;
+  }
 
   const int sm = current_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
@@ -325,7 +332,7 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const int G = a->Hq / a->Hkv;
   const int rows = a->q_len > 0 ? a->q_len : 1;
   const WsLayout w = ws_layout(a->B, a->Hkv, (int64_t)G * rows, a->D, plan.S);
-  if (workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+  if (!kernels && workspace_bytes < w.total) return PA_ERR_WORKSPACE;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   pa::DecodeParams p{};
@@ -372,13 +379,17 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
   const bool bf16 = a->dtype == PA_BF16;
   if (p.kv_fp8) {
     if (a->D == 128)
-      e = bf16 ? pa::launch_decode_fp8_bf16_d128(p, cs) : pa::launch_decode_fp8_f16_d128(p, cs);
+      e = bf16 ? pa::launch_decode_fp8_bf16_d128(p, cs, kernels) : pa::launch_decode_fp8_f16_d128(p, cs, kernels);
     else
-      e = bf16 ? pa::launch_decode_fp8_bf16_d256(p, cs) : pa::launch_decode_fp8_f16_d256(p, cs);
+      e = bf16 ? pa::launch_decode_fp8_bf16_d256(p, cs, kernels) : pa::launch_decode_fp8_f16_d256(p, cs, kernels);
   } else if (a->D == 128) {
-    e = bf16 ? pa::launch_decode_bf16_d128(p, cs) : pa::launch_decode_f16_d128(p, cs);
+    e = bf16 ? pa::launch_decode_bf16_d128(p, cs, kernels) : pa::launch_decode_f16_d128(p, cs, kernels);
   } else {
-    e = bf16 ? pa::launch_decode_bf16_d256(p, cs) : pa::launch_decode_f16_d256(p, cs);
+    e = bf16 ? pa::launch_decode_bf16_d256(p, cs, kernels) : pa::launch_decode_f16_d256(p, cs, kernels);
+  }
+  if (e != cudaSuccess && kernels) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -389,6 +400,16 @@ pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspac
     return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+pa_status pa_decode_ex(const pa_decode_args* a, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
+  return decode_ex(a, workspace, workspace_bytes, stream, nullptr);
+}
+
+pa_status pa_decode_kernel_count(const pa_decode_args* a, int* kernels) {
+  if (!kernels) return PA_ERR_INVALID_ARG;
+  return decode_ex(a, nullptr, 0, nullptr, kernels);
 }
 
 pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,

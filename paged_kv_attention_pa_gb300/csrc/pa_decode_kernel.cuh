@@ -46,6 +46,9 @@
 namespace pa {
 
 constexpr int kSmemBudget = 224 * 1024;
+#ifndef PA_CLUSTER_MERGE_MAX
+#define PA_CLUSTER_MERGE_MAX 8  // largest split count merged in its cluster (2..8)
+#endif
 
 // F8: the cache holds FP8 E4M3 (one byte per element); tiles land in the ring as
 // bytes, and each lane widens the bytes of its MMA fragments in registers.
@@ -81,10 +84,16 @@ __device__ __forceinline__ int div_block(const DecodeParams& p, int t) {
   return p.bs_magic == 0 ? (t >> p.bs_shift) : (int)(__umulhi((uint32_t)t, p.bs_magic) >> p.bs_shift);
 }
 
+// The cluster merge keeps, in the last warp's ring region after that warp's parked
+// state, one receive entry of 12 floats (8 sums, maximum, denominator, padding) per
+// split of the cluster and output item of this split's share: at most
+// (items + splits) entries, items = 8 NT columns x D / 8.
+constexpr int kRecvFloats = 12;
 template <int D, int NT, bool F8>
 __host__ __device__ constexpr bool cluster_merge_fits() {
   using C = Cfg<D, NT, F8>;
-  return D == 128 && (8 * NT * (D + 6) + 8 * NT * D + 16 * NT) * 4 <= C::DEPTH * C::SLOT_BYTES;
+  return (8 * NT * (D + 6) + (8 * NT * (D / 8) + kMaxClusterMerge) * kRecvFloats) * 4 <=
+         C::DEPTH * C::SLOT_BYTES;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
@@ -645,6 +654,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   const bool single = n_splits == 1;
   const size_t pidx = ((size_t)b * p.Hkv + kvh) * p.S + split;
   constexpr int DV = D / 8;  // items per column
+  // The cluster merge: the C = p.cmerge splits of this (sequence, KV head) form one
+  // cluster. Split r owns output items [r per, (r + 1) per); every split pushes its
+  // state of each item into the owner's receive entries (distributed shared memory
+  // stores, which need no round trip), and after a cluster barrier every owner
+  // reduces its items from its own shared memory.
+  const int ccount = p.cmerge;
+  const int cper = ccount ? (cols * DV + ccount - 1) / ccount : 0;
+  float* const recv = wstate(kWarps - 1) + WSTATE;  // [C][cper][kRecvFloats]
+  if constexpr (cluster_merge_fits<D, NT, F8>()) {
+    // every split of the cluster is past its main loop: the receive entries (in ring
+    // memory) are free
+    if (ccount) cluster_sync_relaxed();  // orders execution: nothing is pending on them
+  }
   for (int it = threadIdx.x; it < cols * DV; it += kThreads) {
     const int g = it / DV, d0 = (it % DV) * 8;  // g: column
     float M = -INFINITY;
@@ -667,15 +689,13 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     // cache values are stored values times v_scale (1 unless fp8); a column whose
     // row sees no token of this split has M = -inf and den = 0
     if constexpr (cluster_merge_fits<D, NT, F8>()) {
-      if (p.cmerge) {  // this split's state for the cluster merge below
-        float* xb = wstate(kWarps - 1) + WSTATE;
-        float4* xv = reinterpret_cast<float4*>(xb + g * D + d0);
-        xv[0] = make_float4(v[0], v[1], v[2], v[3]);
-        xv[1] = make_float4(v[4], v[5], v[6], v[7]);
-        if (d0 == 0) {
-          xb[GT * D + g] = M;
-          xb[GT * D + GT + g] = den;
-        }
+      if (ccount) {  // this split's state of the item, pushed to the item's owner
+        const int owner = it / cper;
+        float* e = const_cast<float*>(map_cluster_rank(recv, (uint32_t)owner)) +
+                   ((size_t)cluster_rank() * cper + (it - owner * cper)) * kRecvFloats;
+        reinterpret_cast<float4*>(e)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(e)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        reinterpret_cast<float2*>(e)[4] = make_float2(M, den);
         continue;
       }
     }
@@ -699,38 +719,50 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     }
   }
   if constexpr (cluster_merge_fits<D, NT, F8>()) {
-    if (p.cmerge) {
-      // The two splits of this (sequence, KV head) form one cluster: split 1's state
-      // is read from its shared memory (distributed shared memory) and merged here,
-      // so no partials reach global memory and no merge grid runs.
-      cluster_sync();  // both splits' states are complete
-      if (cluster_rank() == 0) {
-        if (p.Ps < p.P && threadIdx.x == 0) p.steal[(size_t)b * p.Hkv + kvh] = 0;  // no claims left
-        const float* xb = wstate(kWarps - 1) + WSTATE;
-        const uint32_t rx = dsmem_addr(smem_addr(xb), 1);
-        for (int it = threadIdx.x; it < cols * DV; it += kThreads) {
-          const int g = it / DV, d0 = (it % DV) * 8;
-          const float m0 = xb[GT * D + g], l0 = xb[GT * D + GT + g];
-          const float m1 = ld_dsmem_f32(rx + 4u * (GT * D + g));
-          const float l1 = ld_dsmem_f32(rx + 4u * (GT * D + GT + g));
-          const float M = fmaxf(m0, m1);
-          const float w0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M);
-          const float w1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M);
-          const float den = w0 * l0 + w1 * l1;
-          const float r = den > 0.f ? p.v_scale / den : 0.f;
-          const float4* x0 = reinterpret_cast<const float4*>(xb + g * D + d0);
-          const float4 a0 = x0[0], a1 = x0[1];
-          const uint32_t x1 = rx + 4u * (g * D + d0);
-          const float4 c0 = ld_dsmem_f4(x1), c1 = ld_dsmem_f4(x1 + 16u);
-          uint4 pk;
-          pk.x = pack2<T>((w0 * a0.x + w1 * c0.x) * r, (w0 * a0.y + w1 * c0.y) * r);
-          pk.y = pack2<T>((w0 * a0.z + w1 * c0.z) * r, (w0 * a0.w + w1 * c0.w) * r);
-          pk.z = pack2<T>((w0 * a1.x + w1 * c1.x) * r, (w0 * a1.y + w1 * c1.y) * r);
-          pk.w = pack2<T>((w0 * a1.z + w1 * c1.z) * r, (w0 * a1.w + w1 * c1.w) * r);
-          *reinterpret_cast<uint4*>(out + qrow(g) * D + d0) = pk;
+    if (ccount) {
+      cluster_sync();  // every push has landed; no split reads another's memory after this
+      const int rank = (int)cluster_rank();
+      if (rank == 0 && p.Ps < p.P && threadIdx.x == 0)
+        p.steal[(size_t)b * p.Hkv + kvh] = 0;  // no claims left
+      const int i_lo = rank * cper, i_hi = min(cols * DV, i_lo + cper);
+      for (int it = i_lo + threadIdx.x; it < i_hi; it += kThreads) {
+        const int g = it / DV, d0 = (it % DV) * 8;
+        const float* e0 = recv + (size_t)(it - i_lo) * kRecvFloats;
+        // every entry loaded first, then the reduction
+        float2 ml[kMaxClusterMerge];
+        float4 xc[kMaxClusterMerge], yc[kMaxClusterMerge];
+        float M = -INFINITY;
+#pragma unroll
+        for (int c2 = 0; c2 < kMaxClusterMerge; ++c2) {
+          if (c2 < ccount) {
+            const float* e = e0 + (size_t)c2 * cper * kRecvFloats;
+            xc[c2] = reinterpret_cast<const float4*>(e)[0];
+            yc[c2] = reinterpret_cast<const float4*>(e)[1];
+            ml[c2] = reinterpret_cast<const float2*>(e)[4];
+            M = fmaxf(M, ml[c2].x);
+          }
         }
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float den = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < kMaxClusterMerge; ++c2) {
+          if (c2 < ccount) {
+            // a split that saw no token of the column (m = -inf) weighs 0
+            const float w = ml[c2].x == -INFINITY ? 0.f : exp2_approx(ml[c2].x - M);
+            const float4 x = xc[c2], y = yc[c2];
+            den += w * ml[c2].y;
+            v[0] += w * x.x; v[1] += w * x.y; v[2] += w * x.z; v[3] += w * x.w;
+            v[4] += w * y.x; v[5] += w * y.y; v[6] += w * y.z; v[7] += w * y.w;
+          }
+        }
+        const float r = den > 0.f ? p.v_scale / den : 0.f;
+        uint4 pk;
+        pk.x = pack2<T>(v[0] * r, v[1] * r);
+        pk.y = pack2<T>(v[2] * r, v[3] * r);
+        pk.z = pack2<T>(v[4] * r, v[5] * r);
+        pk.w = pack2<T>(v[6] * r, v[7] * r);
+        *reinterpret_cast<uint4*>(out + qrow(g) * D + d0) = pk;
       }
-      cluster_sync();  // split 1's shared memory stays until split 0 has read it
     }
   }
 }
@@ -860,8 +892,9 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
 }
 
 template <typename T, typename KV, int D, int NT, bool WIN>
-cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st, int* kernels) {
   using C = Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>;
+  auto kern = decode_kernel<T, KV, D, NT, WIN>;
   // The dynamic shared memory opt-in is per device; remember which devices have it.
   static unsigned long long done_mask = 0ull;
   int dev = 0;
@@ -869,16 +902,52 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_kernel<T, KV, D, NT, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  // Two splits merge inside their cluster (no merge grid) when their states fit.
   DecodeParams q = p;
-  q.cmerge = (p.S == 2 && cluster_merge_fits<D, NT, std::is_same_v<KV, fp8e4m3>>()) ? 1 : 0;
-  e = launch_pdl(decode_kernel<T, KV, D, NT, WIN>, dim3(q.S, q.Hkv, q.B), dim3(C::THREADS), C::SMEM, st, q,
-                 q.cmerge ? 2u : 1u);
+  // The splits of each (sequence, KV head) merge inside their cluster (no merge grid)
+  // when their states fit: always for two splits; for three to kMaxClusterMerge when
+  // every cluster of the launch is resident at once (clusters of more than two CTAs
+  // pack the SMs less densely, so a launch of several waves keeps the merge grid).
+  q.cmerge = 0;
+  if (cluster_merge_fits<D, NT, std::is_same_v<KV, fp8e4m3>>() && q.S >= 2 &&
+      q.S <= PA_CLUSTER_MERGE_MAX && q.S <= kMaxClusterMerge) {
+    if (q.S == 2) {
+      q.cmerge = 2;
+    } else if (dev < 64) {
+      static int clusters[64][kMaxClusterMerge + 1] = {};  // resident clusters, per size
+      int n = __atomic_load_n(&clusters[dev][q.S], __ATOMIC_ACQUIRE);
+      if (n == 0) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(q.S, q.Hkv, q.B);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = q.S;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int got = 0;
+        if (cudaOccupancyMaxActiveClusters(&got, kern, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          got = 0;
+        }
+        n = got > 0 ? got : -1;
+        __atomic_store_n(&clusters[dev][q.S], n, __ATOMIC_RELEASE);
+      }
+      if (n > 0 && (long long)q.B * q.Hkv <= n) q.cmerge = q.S;
+    }
+  }
+  if (kernels) {  // the count only
+    *kernels = (q.S > 1 && !q.cmerge) ? 2 : 1;
+    return cudaSuccess;
+  }
+  e = launch_pdl(kern, dim3(q.S, q.Hkv, q.B), dim3(C::THREADS), C::SMEM, st, q,
+                 q.cmerge ? (unsigned)q.cmerge : 1u);
   if (e != cudaSuccess) return e;
   if (q.S > 1 && !q.cmerge)
     e = launch_pdl(merge_kernel<T, D>, dim3(D / 64, q.Hq * q.q_len, q.B), dim3(256), 0, st, q);
@@ -888,14 +957,14 @@ cudaError_t launch_decode_nt(const DecodeParams& p, cudaStream_t st) {
 // Column tiles of 8: one for up to 8 (row, head) columns, two for 16, four for 32
 // (head_dim 128 only, no window: the host rejects the rest).
 template <typename T, typename KV, int D>
-cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode_dispatch(const DecodeParams& p, cudaStream_t st, int* kernels) {
   const int cols = p.G * p.q_len;
   if (p.window > 0)
-    return cols <= 8 ? launch_decode_nt<T, KV, D, 1, true>(p, st)
-                     : launch_decode_nt<T, KV, D, 2, true>(p, st);
-  if (cols <= 8) return launch_decode_nt<T, KV, D, 1, false>(p, st);
-  if (cols <= 16 || D != 128) return launch_decode_nt<T, KV, D, 2, false>(p, st);
-  if constexpr (D == 128) return launch_decode_nt<T, KV, D, 4, false>(p, st);
+    return cols <= 8 ? launch_decode_nt<T, KV, D, 1, true>(p, st, kernels)
+                     : launch_decode_nt<T, KV, D, 2, true>(p, st, kernels);
+  if (cols <= 8) return launch_decode_nt<T, KV, D, 1, false>(p, st, kernels);
+  if (cols <= 16 || D != 128) return launch_decode_nt<T, KV, D, 2, false>(p, st, kernels);
+  if constexpr (D == 128) return launch_decode_nt<T, KV, D, 4, false>(p, st, kernels);
   return cudaErrorInvalidValue;
 }
 

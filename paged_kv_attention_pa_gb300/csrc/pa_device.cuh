@@ -68,10 +68,16 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 // and their writes are visible; returns at once for an ordinary launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Thread-block cluster barrier (all threads of every CTA of the cluster): a hardware
-// barrier; release / acquire order the shared-memory writes before it for reads
-// from other CTAs of the cluster after it.
+// barrier; release / acquire order the shared-memory writes before it (to this CTA's
+// memory or another's of the cluster) before every access after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Cluster barrier that orders execution only (relaxed arrive): for handing over
+// memory that no thread of the cluster has accesses pending on.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" :::
                    "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -79,24 +85,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-// Address of the same shared-memory location in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+// Generic address of the same shared-memory object in CTA `rank` of this cluster:
+// plain loads and stores through it reach that CTA's shared memory (distributed
+// shared memory) and are scheduled like any other memory access.
+__device__ __forceinline__ const float* map_cluster_rank(const float* p, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(p), "r"(rank));
+  return reinterpret_cast<const float*>(r);
 }
 // Allow the next grid in the stream to be scheduled (it still waits in pdl_wait).
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -2,7 +2,7 @@
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
-cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st) {
-  return launch_decode_dispatch<__half, __half, 128>(p, st);
+cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st, int* kernels) {
+  return launch_decode_dispatch<__half, __half, 128>(p, st, kernels);
 }
 }  // namespace pa

@@ -2,7 +2,7 @@
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
-cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st) {
-  return launch_decode_dispatch<__half, fp8e4m3, 256>(p, st);
+cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st, int* kernels) {
+  return launch_decode_dispatch<__half, fp8e4m3, 256>(p, st, kernels);
 }
 }  // namespace pa

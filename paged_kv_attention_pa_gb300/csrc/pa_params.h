@@ -66,6 +66,9 @@ constexpr int kStealDiv = PA_STEAL_DIV;
 #endif
 constexpr long long kStealMinBytes = (long long)PA_STEAL_MIN_KIB * 1024;  // K + V bytes per split
 constexpr int kStealUnits = 2048;
+// Largest split count whose splits merge inside their thread-block cluster (the
+// portable cluster size).
+constexpr int kMaxClusterMerge = 8;
 constexpr int kHeaderBytes = 256 + kStealUnits * 4;  // error word, then the counters
 static_assert(kHeaderBytes % 256 == 0, "header keeps 256-byte alignment");
 static_assert(kHeaderBytes == PA_WORKSPACE_HEADER_BYTES, "header size is part of the ABI");
@@ -93,21 +96,24 @@ struct DecodeParams {
   int window;         // > 0: attend to the last `window` tokens only
   int q_len;          // query rows per sequence (causal among themselves)
   int kv_fp8;         // caches hold FP8 E4M3 (k_scale is folded into scale_log2)
-  int cmerge;         // S == 2 launched as clusters of the two splits, which merge in
-                      // distributed shared memory (set by the launcher; no merge grid)
+  int cmerge;         // 0, or C = S: the S splits of each (sequence, KV head) run as one
+                      // thread-block cluster and merge in distributed shared memory (set
+                      // by the launcher; no merge grid)
   float v_scale;      // cache V value = stored value * v_scale
   float scale_log2;   // scale * log2(e): scores live in the exp2 domain
 };
 
-// One launcher per (dtype, head_dim); each dispatches on the GQA group size.
-cudaError_t launch_decode_bf16_d128(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_bf16_d256(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_f16_d256(const DecodeParams& p, cudaStream_t st);
+// One launcher per (dtype, head_dim); each dispatches on the GQA group size. With
+// kernels != nullptr nothing is launched: *kernels is set to the number of kernels
+// the launch would make (1, or 2 with a merge grid).
+cudaError_t launch_decode_bf16_d128(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_bf16_d256(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_f16_d128(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_f16_d256(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
 // FP8 E4M3 caches with bf16 / fp16 queries and outputs.
-cudaError_t launch_decode_fp8_bf16_d128(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_fp8_bf16_d256(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_fp8_f16_d128(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode_fp8_bf16_d128(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_fp8_bf16_d256(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_fp8_f16_d128(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
+cudaError_t launch_decode_fp8_f16_d256(const DecodeParams& p, cudaStream_t st, int* kernels = nullptr);
 
 }  // namespace pa

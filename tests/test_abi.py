@@ -210,3 +210,22 @@ def test_many_pairs_long_context_split_in_two():
     # last of the waves (GB300: 1273 vs 1356 us per call)
     S, P = pa.plan(64, 32, 8, 128, 16, 32768, sm_count=SM)
     assert S == 2 and P == 16384
+
+
+def test_kernel_count_validates_and_launches_nothing(lib):
+    import torch
+    n = ctypes.c_int(-1)
+    # the same argument errors as the decode call, a null result, an empty batch
+    assert lib.pa_decode_kernel_count(ctypes.byref(_args(Hq=12, Hkv=8)), ctypes.byref(n)) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_kernel_count(ctypes.byref(_args(D=64)), ctypes.byref(n)) == \
+        pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode_kernel_count(ctypes.byref(_args()), None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_kernel_count(ctypes.byref(_args(B=0)), ctypes.byref(n)) == pa.PA_OK
+    assert n.value == 0
+    # pointer fields are never read: null pointers are no error here
+    rc = lib.pa_decode_kernel_count(ctypes.byref(_args(q=0, k_cache=0, out=0)), ctypes.byref(n))
+    if torch.cuda.is_available():
+        assert rc == pa.PA_OK and n.value in (1, 2)
+    else:
+        assert rc == pa.PA_ERR_CUDA  # the count depends on the device

@@ -41,26 +41,26 @@ def test_captures_read_each_kv_byte_about_once():
         assert 1.0 <= cap["dram_bytes"] / cap["alg_bytes"] < 1.02, (D, kv)
 
 
-def test_kernels_per_call_follows_the_split_plan(monkeypatch):
-    # one launch without a split; two splits at head_dim 128 merge in their clusters
-    # (one launch); more splits, or two at head_dim 256, add the merge grid
+def test_kernels_per_call_asks_the_library(monkeypatch):
+    # the launch count is the library's own answer for the cell's tensors (which
+    # depends on the device: splits merge in their clusters only when resident)
     import paged_kv_attention_pa_gb300 as pa
+    seen = {}
+
+    def fake_count(q, k, v, bt, sl, scale, max_seq_len=None, window=0, total_tokens=0):
+        seen.update(q=q, k=k, max_seq_len=max_seq_len, window=window, total_tokens=total_tokens)
+        return 2
+
+    class Inst:
+        q, k, v, bt, sl = "q", "k", "v", "bt", "sl"
 
     class Cell:
-        def __init__(self, B, Hq, Hkv, D, bs, L, rows=1):
-            self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
-            self.max_len, self.window, self.total_tokens, self.rows = L, 0, 0, rows
+        insts = [Inst()]
+        scale, max_len, window, total_tokens = 0.0625, 4096, 1024, 8192
 
-    splits = {}
-    monkeypatch.setattr(pa, "plan", lambda B, Hq, Hkv, D, bs, L, **kw: (splits[(D, L)], 64))
-    monkeypatch.setattr(bench, "KV_FP8", False)
-    for (D, S, n) in [(128, 1, 1), (128, 2, 1), (128, 3, 2), (256, 2, 2), (256, 38, 2)]:
-        splits[(D, 4096)] = S
-        assert bench.kernels_per_call(pa, Cell(8, 32, 8, D, 16, 4096)) == n, (D, S)
-    monkeypatch.setattr(bench, "KV_FP8", True)
-    splits[(128, 4096)] = 2
-    assert bench.kernels_per_call(pa, Cell(8, 32, 8, 128, 16, 4096)) == 1
-    assert bench.kernels_per_call(pa, Cell(8, 64, 8, 128, 16, 4096, rows=3)) == 2  # 24 columns
+    monkeypatch.setattr(pa, "kernel_count", fake_count)
+    assert bench.kernels_per_call(pa, Cell()) == 2
+    assert seen == dict(q="q", k="k", max_seq_len=4096, window=1024, total_tokens=8192)
 
 
 def test_curve_summary_picks_the_batch1_and_mixed_cells():

@@ -588,8 +588,8 @@ def test_two_streams_with_their_own_workspaces(cuda_lib):
 @pytest.mark.parametrize("shape", ["d128", "hybrid", "fp8", "window", "rows"])
 def test_two_splits_merge_in_their_cluster(cuda_lib, shape):
     # Two splits run as one thread-block cluster and merge in distributed shared
-    # memory, with no merge grid (head_dim 128; the head_dim-256 shape takes the merge
-    # grid, and must pass the same checks). Edge cases: an empty context, contexts where the
+    # memory, with no merge grid (both head_dims; fp8 caches with more than 16 columns
+    # at head_dim 128 take the merge grid). Edge cases: an empty context, contexts where the
     # second split has no token (one of them, 1900, ends between the second split's
     # static start and the partition size, where a split past the sequence would
     # double-count tokens if it streamed its static share), a context shorter than a
@@ -624,6 +624,50 @@ def test_two_splits_merge_in_their_cluster(cuda_lib, shape):
     b = run(cuda_lib, case, deterministic=True, **kw)
     assert torch.equal(a, b)
     no_device_errors(cuda_lib)
+
+
+@pytest.mark.parametrize("S", [3, 5, 8])
+@pytest.mark.parametrize("shape", ["d128", "hybrid", "fp8"])
+def test_splits_merge_in_their_cluster(cuda_lib, S, shape):
+    # Three to eight splits of each (sequence, KV head) run as one thread-block
+    # cluster when every cluster of the launch is resident at once: each split pushes
+    # its state of every output item into the item's owner (distributed shared
+    # memory) and the owners reduce, with no merge grid. Edge cases as for two splits:
+    # an empty context, splits past the sequence, a context shorter than a tile.
+    lens = [0, 5, 33, 700, 1900]
+    if shape == "hybrid":  # 3 sequences x 4 KV heads: 12 clusters, all resident
+        case = pi.make_case(3, 24, 4, 256, 784, [0, 33, 1900], seed=40 + S, poison="kv_nan")
+    elif shape == "fp8":
+        case = pi.make_case(5, 16, 2, 128, 16, lens, seed=41 + S, poison="kv_nan", kv_dtype="fp8")
+    else:
+        case = pi.make_case(5, 8, 2, 128, 16, lens, seed=42 + S, poison="kv_nan")
+    c = case.to("cuda")
+    assert cuda_lib.kernel_count(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens, c.scale,
+                                 max_seq_len=c.max_seq_len, splits=S) == 1, "no merge grid"
+    y = run(cuda_lib, c, splits=S)
+    ref = oracle_case(case)
+    assert_parity(to_np(y), ref, what=f"{S} splits in a cluster, {shape}")
+    assert float(y[0].abs().max()) == 0.0  # the empty context
+    # the merge grid (more splits than a cluster takes) agrees
+    assert rel_diff(y, run(cuda_lib, c, splits=12)) <= ORDER_TOL
+    a = run(cuda_lib, c, splits=S, deterministic=True)
+    assert torch.equal(a, run(cuda_lib, c, splits=S, deterministic=True))
+    no_device_errors(cuda_lib)
+
+
+def test_kernel_count_follows_the_plan(cuda_lib):
+    # one kernel for a single split or splits merging in their cluster, two with a
+    # merge grid; the bench counts its launches through this call
+    def count(B, hq, hkv, D, bs, L, **kw):
+        c = pi.make_case(B, hq, hkv, D, bs, [L] * B, seed=7, device="cuda")
+        return cuda_lib.kernel_count(c.q, c.k_cache, c.v_cache, c.block_tables, c.seq_lens,
+                                     c.scale, max_seq_len=L, **kw)
+    assert count(8, 32, 16, 128, 16, 8192) == 1          # one split per sequence
+    assert count(8, 8, 8, 128, 16, 4096) == 1            # two splits, merged in clusters
+    assert count(1, 24, 4, 256, 784, 500) == 1           # eight splits, four clusters
+    assert count(1, 8, 8, 128, 16, 4096) == 2            # 19 splits: the merge grid
+    assert count(8, 8, 8, 128, 16, 32768) == 2           # 7 splits of 64 pairs: not resident
+    assert count(2, 8, 8, 128, 16, 4096, splits=1) == 1
 
 
 def test_dependent_calls_back_to_back(cuda_lib):
