@@ -253,14 +253,14 @@ def load_peaks():
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
 # A capture holds only for the kernel sources it was taken on: when their SHA-256
 # differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "dca3d947cc5a0ce76faa5e377464bf8828e94c5938a0deb5ad645efb515a4bcf"
+TRAFFIC_SOURCES_SHA256 = "e99748fa3df84e4980bae04573c420b913c9099fca769565ac7f35917f54a006"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
-    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537051989 + 1438549},
+    (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537060778 + 1362773},
     # 24q/4kv, block 784, batch 1, 32768 tokens: three launches
-    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134300245 + 908971},
+    (256, "bf16"): {"alg_bytes": 134217728, "dram_bytes": 134300074 + 949077},
     # 32q/8kv fp8 E4M3 KV, block 16, batch 8, 16384 tokens: three launches
-    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268600064 + 1107371},
+    (128, "fp8"): {"alg_bytes": 268435456, "dram_bytes": 268605440 + 955136},
 }
 
 
