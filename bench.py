@@ -251,9 +251,10 @@ def load_peaks():
 # DRAM traffic of decode_kernel per algorithmic KV byte, from ncu captures of single
 # cells (dram__bytes_read.sum + dram__bytes_write.sum, mean over the captured
 # launches), keyed by (head_dim, KV type) and scaled to a call by its KV bytes.
-# A capture holds only for the kernel sources it was taken on: when their SHA-256
-# differs from the one recorded here, the bench reports traffic as null.
-TRAFFIC_SOURCES_SHA256 = "e99748fa3df84e4980bae04573c420b913c9099fca769565ac7f35917f54a006"
+# A capture holds only for the kernel code it was taken on: when the SHA-256 of that
+# code (comments and blank space removed) differs from the one recorded here, the
+# bench reports traffic as null.
+TRAFFIC_SOURCES_SHA256 = "2c6c9c40854a25d0cb3fe75642fe0c9c19b9f6e7319ab9d206456f57653b56e1"
 TRAFFIC_CAPTURES = {
     # 32q/8kv, block 16, batch 8, 16384 tokens: three launches
     (128, "bf16"): {"alg_bytes": 536870912, "dram_bytes": 537060778 + 1362773},
@@ -264,18 +265,27 @@ TRAFFIC_CAPTURES = {
 }
 
 
-def kernel_sources_sha256() -> str:
-    """SHA-256 of the device code: the kernel headers, the launch parameters and the
-    instantiation units (host-side planning and the C API are not part of it)."""
+def code_tokens(src: str) -> str:
+    """C/C++/CUDA source with comments and blank space removed: what the compiler
+    sees of it, so that edits to comments leave a fingerprint unchanged."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_sources_sha256(csrc=None) -> str:
+    """SHA-256 of the device code (comments and blank space removed): the kernel
+    headers, the launch parameters and the instantiation units (host-side planning
+    and the C API are not part of it)."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_kv_attention_pa_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_kv_attention_pa_gb300", "csrc")
     files = sorted(f for f in os.listdir(csrc)
                    if f.endswith(".cuh") or f == "pa_params.h" or f.startswith("pa_inst_"))
     for f in files:
         h.update(f.encode())
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()
 
 
@@ -838,7 +848,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "traffic_source": traffic_note,
                      "peak_kind": peak_kind,
-                     "kernel": "pa::decode_kernel (+ pa::merge_kernel when split in more than two)",
+                     "kernel": "pa::decode_kernel (+ pa::merge_kernel where the splits do not merge in their clusters)",
                      "alg_bytes_per_launch": round(alg / len(cells)),
                      "avg_launch_us": round(1e3 * ms_step_max / len(cells), 3),
                      "launch_timing": "timed region / decode calls (graph replay, "

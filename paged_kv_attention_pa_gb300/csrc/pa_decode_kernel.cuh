@@ -29,11 +29,11 @@
 // fragments.
 //
 // Epilogue: the warps merge their (m, l, acc) in shared memory. A sequence that
-// fits in one split gets its output written here. Two splits at head_dim 128 run
-// as one thread-block cluster and merge through distributed shared memory.
-// Otherwise the split's partial goes to the workspace and merge_kernel, chained
-// behind this grid with a programmatic dependent launch, combines the splits of
-// every (sequence, head) in parallel.
+// fits in one split gets its output written here. Up to eight splits of a
+// (sequence, KV head) can run as one thread-block cluster and merge through
+// distributed shared memory. Otherwise the split's partial goes to the workspace
+// and merge_kernel, chained behind this grid with a programmatic dependent launch,
+// combines the splits of every (sequence, head) in parallel.
 #pragma once
 
 #include <cstdint>
@@ -75,10 +75,6 @@ struct Cfg {
   static_assert(DEPTH >= 2, "need at least two slots per warp");
 };
 
-// The two-split cluster merge: at head_dim 128, where one warp's ring region holds,
-// after the last warp's merged state, a split's whole output state ([GT][D] sums,
-// then GT maxima and GT denominators). (Compiled into the head_dim-256 kernels it
-// cost the hybrid layer ~0.2 us per call, which never splits in two.)
 // t / block_size for a token index 0 <= t < 2^31 (see bs_magic)
 __device__ __forceinline__ int div_block(const DecodeParams& p, int t) {
   return p.bs_magic == 0 ? (t >> p.bs_shift) : (int)(__umulhi((uint32_t)t, p.bs_magic) >> p.bs_shift);

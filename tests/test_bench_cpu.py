@@ -36,6 +36,14 @@ def test_traffic_is_null_once_the_device_code_changes(monkeypatch):
     assert t is None and "changed" in note
 
 
+def test_source_fingerprint_ignores_comments_not_code():
+    a = "int f(int x) {\n  return x + 1;  // one more\n}\n/* block\n comment */\n"
+    b = "int f(int x) { return x + 1; }  // reworded comment\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench.code_tokens(a) == bench.code_tokens(b) == "int f(int x) { return x + 1; }"
+    assert bench.code_tokens(c) != bench.code_tokens(a)
+
+
 def test_captures_read_each_kv_byte_about_once():
     for (D, kv), cap in bench.TRAFFIC_CAPTURES.items():
         assert 1.0 <= cap["dram_bytes"] / cap["alg_bytes"] < 1.02, (D, kv)
