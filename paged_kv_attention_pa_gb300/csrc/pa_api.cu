@@ -40,6 +40,9 @@ struct Plan {
 #define PA_SPLIT_OVERHEAD_BYTES (256 << 10)
 #endif
 constexpr int64_t kSplitOverheadBytes = PA_SPLIT_OVERHEAD_BYTES;
+#ifndef PA_PLAN_BALANCED
+#define PA_PLAN_BALANCED 1
+#endif
 
 bool plan_for(int64_t S_req, int64_t max_len, int64_t p_max, bool floor_p, int64_t quantum,
               Plan* out) {
@@ -80,19 +83,29 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t kv_elem_
     if (total_tokens <= 0) return all;
     return std::min(all, Hkv * (ceil_div(total_tokens, pl.P) + ceil_div(B, 2)));
   };
-  for (int64_t c : cands) {
-    if (c < 1) continue;
-    Plan pl{};
-    if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
+  // A CTA streams its split as rounds of one tile per warp, so its time follows
+  // the tokens rounded up to whole rounds; a split of that rounded size is as fast
+  // and needs fewer CTAs, which is also tried for every candidate.
+  const int64_t round_tokens =
+      quantum * (PA_PLAN_BALANCED ? pa::warps_per_cta((int)D, kv_elem_bytes == 1) : 1);
+  auto consider = [&](const Plan& pl) {
     const int64_t waves = ceil_div(live_ctas(pl), sm);
     // the fixed cost in tokens of this cache: K + V bytes per token per KV head
     const int64_t overhead_tokens = kSplitOverheadBytes / (2 * D * kv_elem_bytes);
-    const int64_t cost = waves * (pl.P + overhead_tokens);
+    const int64_t cost = waves * (round_up(pl.P, round_tokens) + overhead_tokens);
     if (!found || cost < best_cost || (cost == best_cost && pl.S < out->S)) {
       *out = pl;
       best_cost = cost;
       found = true;
     }
+  };
+  for (int64_t c : cands) {
+    if (c < 1) continue;
+    Plan pl{};
+    if (!plan_for(c, max_len, p_max, true, quantum, &pl)) continue;
+    consider(pl);
+    const int64_t pr = std::min(round_up(pl.P, round_tokens), p_max);
+    if (pr != pl.P) consider(Plan{(int)ceil_div(max_len, pr), (int)pr});
   }
   return found;
 }

@@ -149,10 +149,25 @@ def test_plan_properties(lib, B, Hkv, bs, L):
 
 
 def test_plan_fills_sms_at_batch_one():
+    # one wave, every warp of a CTA streaming the same number of 16-token tiles
+    # (4 warps: splits of whole 64-token rounds)
     S, P = pa.plan(1, 24, 4, 256, 784, 32768, sm_count=SM)
-    assert 4 * S == SM            # one full wave: 37 splits of 896 tokens
+    assert (S, P) == (37, 896) and 4 * S <= SM
     S, P = pa.plan(1, 24, 4, 256, 784, 4096, sm_count=SM)
-    assert 4 * S <= SM and P == 112   # one wave of 112-token splits
+    assert (S, P) == (32, 128)
+
+
+def test_plan_rounds_splits_to_whole_warp_rounds():
+    # A split of 7 tiles keeps three warps busy for two tiles and one for one; 8 tiles
+    # take as long on fewer CTAs (GB300, us per call: 8/8 heads at batch 1, 4K: 6.60
+    # for 16 splits of 256 tokens against 6.87 for 19 of 224; 8K: 9.11 against 9.87;
+    # the hybrid layer at 8K: 10.01 for 32 splits of 256 against 10.57 for 38 of 224)
+    assert pa.plan(1, 8, 8, 128, 16, 4096, sm_count=SM) == (16, 256)
+    assert pa.plan(1, 8, 8, 128, 16, 8192, sm_count=SM) == (16, 512)
+    assert pa.plan(1, 24, 4, 256, 784, 8192, sm_count=SM) == (32, 256)
+    for B, Hkv, D, L in [(1, 8, 128, 4096), (1, 4, 256, 12288), (8, 8, 128, 16384)]:
+        S, P = pa.plan(B, 2 * Hkv, Hkv, D, 16, L, sm_count=SM)
+        assert P % (4 * (32 if D == 128 else 16)) == 0 and S * P >= L
 
 
 def test_forced_splits():
@@ -181,11 +196,12 @@ def test_large_batch_plans():
     assert pa.plan(128, 32, 8, 128, 16, 2048, sm_count=SM)[0] == 1
 
 
-def test_batch8_long_contexts_fill_three_waves():
-    # 64 pairs: three full waves of seven splits beat one wave of two at 16K-32K
-    # (GB300: 87.5 vs 93.0 us at 16K, 163.6 vs 174.0 us at 32K)
-    for L in (16384, 32768):
-        assert pa.plan(8, 32, 8, 128, 16, L, sm_count=SM)[0] == 7
+def test_batch8_long_contexts():
+    # 64 pairs: at 32K three full waves of seven splits beat one wave of two (GB300:
+    # 166.4-169.8 vs 170.5 us); at 16K one wave of two splits, merging in their
+    # clusters, is as fast or faster (86.1-86.5 vs 88.4-90.1 us for seven)
+    assert pa.plan(8, 32, 8, 128, 16, 32768, sm_count=SM)[0] == 7
+    assert pa.plan(8, 32, 8, 128, 16, 16384, sm_count=SM)[0] == 2
     assert pa.plan(8, 8, 8, 128, 16, 4096, sm_count=SM)[0] == 2  # 27.2 us, the best
 
 
