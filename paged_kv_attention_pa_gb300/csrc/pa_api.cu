@@ -83,11 +83,13 @@ bool make_plan(int sm_count, int64_t B, int64_t Hkv, int64_t D, int64_t kv_elem_
     if (total_tokens <= 0) return all;
     return std::min(all, Hkv * (ceil_div(total_tokens, pl.P) + ceil_div(B, 2)));
   };
-  // A CTA streams its split as rounds of one tile per warp, so its time follows
-  // the tokens rounded up to whole rounds; a split of that rounded size is as fast
-  // and needs fewer CTAs, which is also tried for every candidate.
+  // A CTA streams its split as rounds of one tile per warp, so with a 16-bit cache
+  // its time follows the tokens rounded up to whole rounds; a split of that rounded
+  // size is as fast and needs fewer CTAs, which is also tried for every candidate.
+  // An fp8 CTA is bound by its SM's instruction issue, so its time follows all its
+  // tiles: no rounding there (rounded, the fp8 grid and hybrid steps lost 0.5-1%).
   const int64_t round_tokens =
-      quantum * (PA_PLAN_BALANCED ? pa::warps_per_cta((int)D, kv_elem_bytes == 1) : 1);
+      quantum * (PA_PLAN_BALANCED && kv_elem_bytes == 2 ? pa::warps_per_cta((int)D, false) : 1);
   auto consider = [&](const Plan& pl) {
     const int64_t waves = ceil_div(live_ctas(pl), sm);
     // the fixed cost in tokens of this cache: K + V bytes per token per KV head
