@@ -377,6 +377,8 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
   const uint32_t k_lane = (uint32_t)(((lane & 7) + 8 * ((lane >> 3) & 1)) * C::ROWB + (lane >> 4) * 16);
   const uint32_t v_lane = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * C::ROWB + ((lane >> 3) & 1) * 16);
   const float sl2 = p.scale_log2;
+  constexpr bool kLazy = F8;                 // see the rescaling in the softmax
+  constexpr float kSlack = kLazy ? 8.f : 0.f;  // log2 units
 
   for (int k = 0; tq[0] >= 0; ++k) {  // tile k of the stream: tokens tq[0] ..
     const int entry = next_entry;
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
     uint32_t pb[MT][NT][2];
     float x[NT][MT][4];
     float mx[NT][2];
-    bool grow = false;  // some column of this lane sees a score above its running max
+    bool grow = false;  // some column of this lane sees a score above its running max (+ slack)
     if (t0 + C::TW <= L - R + 1) {
       // every token of the tile is below every column's limit (the usual case): no mask
 #pragma unroll
@@ -486,13 +488,19 @@ __global__ void __launch_bounds__(Cfg<D, NT, std::is_same_v<KV, fp8e4m3>>::THREA
         mx[nt][0] = fmaxf(mx[nt][0], fmaxf(x[nt][mt][0], x[nt][mt][2]));
         mx[nt][1] = fmaxf(mx[nt][1], fmaxf(x[nt][mt][1], x[nt][mt][3]));
       }
-      grow = grow || mx[nt][0] > m[nt][0] || mx[nt][1] > m[nt][1];
+      grow = grow || mx[nt][0] > m[nt][0] + kSlack || mx[nt][1] > m[nt][1] + kSlack;
     }
-    // Most tiles raise no running max (all scale factors are exactly 1): they skip
-    // the cross-lane maxima and the rescaling, with bit-identical results. At
-    // head_dim 256, and with more than 8 columns, the skip measured slower per call:
-    // every tile rescales there.
-    const bool rescale = D != 128 || NT > 1 || __any_sync(0xffffffffu, grow);
+    // 16-bit caches: most tiles raise no running max (all scale factors are exactly
+    // 1) and skip the cross-lane maxima and the rescaling, with bit-identical
+    // results; at head_dim 256, and with more than 8 columns, the skip measured
+    // slower per call: every tile rescales there.
+    // FP8 caches (bound by instruction issue): the running max is a reference point,
+    // not necessarily the maximum. Weights are 2^(s - m) against the m in use and the
+    // sums and accumulators stay relative to the same m, so any m gives the same
+    // softmax; m is raised only when a score exceeds it by more than kSlack (weights
+    // stay <= 2^kSlack, exact in fp32 and rounded like any weight to fp16), so
+    // almost every tile skips the rescaling.
+    const bool rescale = (!kLazy && (D != 128 || NT > 1)) || __any_sync(0xffffffffu, grow);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float al0 = 1.f, al1 = 1.f;
