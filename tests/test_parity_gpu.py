@@ -868,6 +868,47 @@ def test_fp8_cache_wide_column_tiles(cuda_lib, dtype, R, hq, hkv, D, bs):
     no_device_errors(cuda_lib)
 
 
+# The fp8 kernels move a column's running max only when a score exceeds it by more
+# than 8 (log2 units), so weights reach 2^8 against a stale max. Keys along one
+# direction with a growing coefficient make scores climb slowly across tiles (many
+# tiles under the slack, then a rescale), jump (one tile far above), or fall (the max
+# stays at the start); heads whose query points the other way see the mirror image.
+def fp8_ramp_case(shape, hq, hkv, D, bs, lens, seed, R=1):
+    kw = dict(seed=seed, kv_dtype="fp8", k_scale=1.0, poison="kv_nan")
+    case = rows_case(R, len(lens), hq, hkv, D, bs, lens, **kw) if R > 1 else \
+        pi.make_case(len(lens), hq, hkv, D, bs, lens, **kw)
+    g = torch.Generator().manual_seed(seed)
+    for b, L in enumerate(lens):
+        t = torch.arange(L, dtype=torch.float32)
+        if shape == "ramp":      # 0 .. 400 over the context
+            a = 400.0 * t / max(L - 1, 1)
+        elif shape == "jump":    # flat, then 300 higher from the middle on
+            a = torch.where(t < L // 2, torch.zeros_like(t), torch.full_like(t, 300.0))
+        else:                    # "fall": 400 down to 0
+            a = 400.0 * (1.0 - t / max(L - 1, 1))
+        k = torch.randn((L, hkv, D), generator=g)
+        k[:, :, 0] = a[:, None]  # d = 0 carries the trend; e4m3 holds it coarsely
+        codes = k.to(pi.FP8)     # k_scale = 1: stored values are the keys
+        case.K[b] = codes
+        bt = case.block_tables[b].long()
+        phys = bt[t.long() // bs]
+        case.k_cache[phys, t.long() % bs] = codes
+    return case
+
+
+@pytest.mark.parametrize("shape", ["ramp", "jump", "fall"])
+@pytest.mark.parametrize("R,hq,hkv,D,bs", [(1, 32, 8, 128, 16), (1, 24, 4, 256, 784),
+                                           (8, 32, 8, 128, 16)])
+def test_fp8_rescale_slack(cuda_lib, shape, R, hq, hkv, D, bs):
+    lens = [4097, 1500] if D == 128 else [5000, 1567]
+    case = fp8_ramp_case(shape, hq, hkv, D, bs, lens, seed=120, R=R).to("cuda")
+    ref = oracle_rows_case(case) if R > 1 else oracle_case(case)
+    for S in (0, 1, 3):
+        y = run(cuda_lib, case, splits=S)
+        assert_parity(to_np(y), ref, what=f"fp8 {shape} R={R} {hq}/{hkv} D={D} splits={S}")
+    no_device_errors(cuda_lib)
+
+
 # ------------------------------------------------------------------ several query rows
 def rows_case(R, *args, **kw):
     """A case whose q holds R query rows per sequence: [B, R, Hq, D]."""
